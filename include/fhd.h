@@ -1,0 +1,186 @@
+/*
+ * fhd.h - C ABI of the GB300 library for the non-uniform Fourier sums of
+ * iterative non-Cartesian MRI reconstruction.
+ *
+ * Source of the operations: "Case study - iterative MRI reconstruction"
+ * (PMPP chapter 17 study notes):
+ *   - section 17.2: the reconstruction minimises ||F rho - D||^2 + lambda R(rho)
+ *     by conjugate gradients, whose inner loop applies F^H D and F^H F rho;
+ *   - section 17.3: rho_n = sum_m D_m exp(i 2 pi k_m . x_n), with the complex
+ *     multiply-accumulate of the gather kernel in 17.3.1
+ *     (re += Dr cos - Di sin, im += Dr sin + Di cos);
+ *   - section 17.3.2: loop fission - per-sample quantities are prepared in a
+ *     separate pass, and F^H F rho runs as two kernels
+ *     (image -> k-space, then k-space -> image).
+ * and "Chapter 17: MRI Reconstruction" (mtuann PMPP notes), step 1 (gather
+ * instead of scatter) and step 4 (samples as an array of structures).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Units      voxel coordinates x, y, z in field-of-view units; sample
+ *            coordinates kx, ky, kz in cycles per field of view; the phase of
+ *            a (voxel, sample) pair is 2 pi (kx x + ky y + kz z) radians.
+ *            There is no normalisation, density compensation or coil weight.
+ * Layout     every array is a contiguous float32 device array (structure of
+ *            arrays); complex values are split into separate real and
+ *            imaginary arrays.  Element i of each array belongs to voxel i
+ *            (length N) or sample i (length M).
+ * Alignment  every array pointer must be 4-byte aligned; the workspace must be
+ *            256-byte aligned.
+ * Ownership  all pointers are owned by the caller and must be device memory
+ *            of the current CUDA device (cudaMalloc'd or managed).  The
+ *            library allocates no memory, keeps no pointer after a call
+ *            returns and holds no global state.
+ * Outputs    are overwritten, never accumulated into.  Outputs must not
+ *            overlap any input, each other, or the workspace.
+ * Async      a call validates its arguments on the host, enqueues its kernels
+ *            on `stream` and returns without synchronising.  Results (and the
+ *            workspace status word) are valid once the stream has completed.
+ *            NULL is the legacy default stream.
+ * Errors     returned as an fhd_status, never thrown.  Argument errors are
+ *            detected on the host before anything is launched, and then
+ *            nothing is written.  A CUDA error raised while enqueueing returns
+ *            FHD_ERR_CUDA.  A kernel whose internal pipeline wait exceeded its
+ *            time limit (about one second) records FHD_ERR_TIMEOUT in the
+ *            workspace status word and exits early; read it with
+ *            fhd_workspace_status() after synchronising.
+ * Modes      FHD_MODE_ACCURATE evaluates sin/cos with sincospif on the
+ *            period-reduced phase (relative L2 error vs an fp64 evaluation
+ *            below 1e-5 on the benchmark workloads).  FHD_MODE_FAST uses the
+ *            hardware sin/cos approximations on the period-reduced phase,
+ *            partly replaced by an FMA-pipe polynomial (relative L2 error
+ *            below 1e-3).
+ * Results are bit-identical from run to run on the same device: the sample
+ * dimension is split among CTAs in a fixed way and the partial sums are
+ * added in a fixed order, without atomics.
+ */
+#ifndef FHD_H
+#define FHD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *fhd_stream_t;
+
+typedef enum {
+    FHD_OK = 0,
+    FHD_ERR_INVALID_VALUE = 1, /* negative size, NULL pointer, unknown mode/op, or not device memory */
+    FHD_ERR_MISALIGNED = 2,    /* array not 4-byte aligned, or workspace not 256-byte aligned */
+    FHD_ERR_ALIAS = 3,         /* an output overlaps an input, another output or the workspace */
+    FHD_ERR_WORKSPACE = 4,     /* workspace smaller than fhd_workspace_bytes() */
+    FHD_ERR_CUDA = 5,          /* a CUDA runtime call failed (see cudaGetLastError) */
+    FHD_ERR_TIMEOUT = 6,       /* a kernel's bounded pipeline wait expired (status word) */
+    FHD_ERR_RANGE = 7          /* an array extends past the end of its device allocation */
+} fhd_status;
+
+typedef enum {
+    FHD_MODE_ACCURATE = 0,
+    FHD_MODE_FAST = 1
+} fhd_mode;
+
+typedef enum {
+    FHD_OP_FHD = 0, /* fhd_compute  */
+    FHD_OP_FWD = 1, /* fwd_compute  */
+    FHD_OP_FHF = 2  /* fhfrho_apply */
+} fhd_op;
+
+/*
+ * Workspace size in bytes that `op` needs for N voxels and M samples on CUDA
+ * device `device` (it depends on the device's SM count).  Returns 0 for an
+ * invalid op, negative sizes or an unknown device.  The same workspace may be
+ * reused by later calls on the same stream.
+ */
+size_t fhd_workspace_bytes(fhd_op op, int64_t N, int64_t M, int device);
+
+/*
+ * Adjoint non-uniform Fourier sum F^H D (section 17.3, the rho_n equation):
+ *
+ *     rho_n = sum_{m=0}^{M-1} D_m exp(+i 2 pi (kx_m x_n + ky_m y_n + kz_m z_n))
+ *
+ * for n = 0..N-1.  Inputs: M samples kx, ky, kz, Dr, Di (length M each) and N
+ * voxels x, y, z (length N each).  Outputs: rho_r, rho_i (length N).
+ * M == 0 writes zeros; N == 0 does nothing (pointers may then be NULL).
+ */
+fhd_status fhd_compute(int64_t M, const float *kx, const float *ky, const float *kz,
+                       const float *Dr, const float *Di,
+                       int64_t N, const float *x, const float *y, const float *z,
+                       float *rho_r, float *rho_i, fhd_mode mode,
+                       void *workspace, size_t workspace_bytes, fhd_stream_t stream);
+
+/* Same type as cudaEvent_t. */
+typedef struct CUevent_st *fhd_event_t;
+
+/*
+ * fhd_compute, additionally recording `gather_start` on `stream` just before
+ * the gather kernel is launched and `gather_stop` just after its fix-up kernel
+ * (the sample-pack kernel runs before `gather_start`).  Either event may be
+ * NULL.  Used to time the dominant kernel inside a larger timed region.
+ */
+fhd_status fhd_compute_profiled(int64_t M, const float *kx, const float *ky, const float *kz,
+                                const float *Dr, const float *Di,
+                                int64_t N, const float *x, const float *y, const float *z,
+                                float *rho_r, float *rho_i, fhd_mode mode,
+                                void *workspace, size_t workspace_bytes, fhd_stream_t stream,
+                                fhd_event_t gather_start, fhd_event_t gather_stop);
+
+/*
+ * Forward non-uniform Fourier sum F rho (the image -> k-space operator of
+ * section 17.2; its kernel is the conjugate of the adjoint's):
+ *
+ *     D_m = sum_{n=0}^{N-1} rho_n exp(-i 2 pi (kx_m x_n + ky_m y_n + kz_m z_n))
+ *
+ * for m = 0..M-1, gathered per sample.  Inputs: N voxels x, y, z, rho_r, rho_i
+ * and M sample coordinates kx, ky, kz.  Outputs: Dr, Di (length M).
+ * N == 0 writes zeros; M == 0 does nothing.
+ */
+fhd_status fwd_compute(int64_t N, const float *x, const float *y, const float *z,
+                       const float *rho_r, const float *rho_i,
+                       int64_t M, const float *kx, const float *ky, const float *kz,
+                       float *Dr, float *Di, fhd_mode mode,
+                       void *workspace, size_t workspace_bytes, fhd_stream_t stream);
+
+/*
+ * Normal operator of the conjugate-gradient loop, out = F^H F rho
+ * (section 17.2; section 17.3.2 splits it into the forward pass and the
+ * adjoint pass as two kernels).  F rho is held in the workspace as float32.
+ * Inputs: N voxels x, y, z, rho_r, rho_i and M sample coordinates.
+ * Outputs: out_r, out_i (length N).  M == 0 writes zeros; N == 0 does nothing.
+ */
+fhd_status fhfrho_apply(int64_t N, const float *x, const float *y, const float *z,
+                        const float *rho_r, const float *rho_i,
+                        int64_t M, const float *kx, const float *ky, const float *kz,
+                        float *out_r, float *out_i, fhd_mode mode,
+                        void *workspace, size_t workspace_bytes, fhd_stream_t stream);
+
+/*
+ * Status word of the last call that used `workspace`: synchronises `stream`,
+ * reads the word and returns FHD_OK or FHD_ERR_TIMEOUT (FHD_ERR_CUDA if the
+ * read fails, FHD_ERR_INVALID_VALUE for a NULL workspace).
+ */
+fhd_status fhd_workspace_status(const void *workspace, fhd_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *fhd_status_string(fhd_status status);
+
+/*
+ * Launch shape the sums use on `device`: CTAs per launch (one persistent CTA
+ * per resident slot), consumer threads per CTA, targets per thread, sources
+ * per staged tile and pipeline stages.  Any pointer may be NULL.  Returns
+ * FHD_ERR_INVALID_VALUE for an unknown device.
+ */
+fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *threads,
+                            int *targets_per_thread, int *tile_sources, int *stages);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int fhd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FHD_H */

@@ -1,0 +1,59 @@
+/*
+ * fhd_testing.h - test-only entry point of the fhd library.
+ *
+ * Not part of the operator API in fhd.h; it exists so the test-suite can
+ * exercise the bounded-wait failure path without faulting or hanging a GPU.
+ * The library has no counterpart of this on the pages it implements.
+ */
+#ifndef FHD_TESTING_H
+#define FHD_TESTING_H
+
+#include "fhd.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * fhd_compute (same arguments, layout and validation), except that the
+ * producer warp of the gather kernel never issues the shared-memory copy of
+ * work item `skip_tile` (a (target block, source tile) index in the kernel's
+ * schedule; -1 skips nothing).  The consumers waiting for that tile then hit
+ * their bounded-wait limit (about one second), set the timeout bit in the
+ * workspace status word and leave; the producer drains its other copies and
+ * leaves.  fhd_workspace_status() then returns FHD_ERR_TIMEOUT and the CUDA
+ * context stays usable.  Output contents are unspecified after a timeout.
+ */
+fhd_status fhd_test_compute_skip_tile(int64_t M, const float *kx, const float *ky, const float *kz,
+                                      const float *Dr, const float *Di,
+                                      int64_t N, const float *x, const float *y, const float *z,
+                                      float *rho_r, float *rho_i, fhd_mode mode,
+                                      void *workspace, size_t workspace_bytes, fhd_stream_t stream,
+                                      int64_t skip_tile);
+
+/*
+ * Host-side replay of the gather schedule for n_targets targets, n_sources
+ * sources and `ctas` persistent CTAs (capped at the number of work items),
+ * using the same schedule functions as the kernels.  Returns 0 when every CTA
+ * owns at least one work item, every target block is finished exactly once
+ * (written whole by one CTA, or summed by exactly one fix-up owner), and each
+ * fix-up's contributors cover the block's source tiles once, in order;
+ * otherwise a positive code naming the first violated property.  Makes no
+ * CUDA call.
+ */
+int fhd_test_schedule(int64_t n_targets, int64_t n_sources, int ctas);
+
+/*
+ * The per-array check every operator applies before launching: `p` must be
+ * non-NULL, 4-byte aligned, device (or managed) memory of `device`, and
+ * [p, p + bytes) must lie inside p's allocation.  Returns FHD_OK,
+ * FHD_ERR_INVALID_VALUE, FHD_ERR_MISALIGNED or FHD_ERR_RANGE; launches
+ * nothing, so a rejected pointer is never dereferenced.
+ */
+fhd_status fhd_test_check_array(const void *p, size_t bytes, int device);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FHD_TESTING_H */

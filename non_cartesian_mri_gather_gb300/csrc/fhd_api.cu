@@ -1,0 +1,457 @@
+// fhd_api.cu - C ABI of the library: argument validation, workspace layout and
+// kernel launches.  Declarations and the contract are in include/fhd.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "../../include/fhd.h"
+#include "../../include/fhd_testing.h"
+#include "fhd_kernels.cuh"
+
+namespace {
+
+using namespace fhd;
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr size_t kWsAlign = 256;
+constexpr size_t kHeaderBytes = 256;  // status word + reserved
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Layout {
+    size_t packed;   // offset of packed source records
+    size_t partial;  // offset of per-CTA partial slots
+    size_t frho;     // offset of F rho (fhfrho_apply only)
+    size_t total;
+};
+
+// Resident CTAs of the gather kernel on `device` (SMs x CTAs per SM).
+cudaError_t max_ctas(int device, fhd_mode mode, int* out) {
+    int sms = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    const size_t smem = sizeof(GatherSmem);
+    if (mode == FHD_MODE_FAST)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<kFast>, kCtaThreads, smem);
+    else
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<kAccurate>, kCtaThreads, smem);
+    if (e != cudaSuccess) return e;
+    per_sm = std::min(std::max(per_sm, 1), kMinCtasPerSm);
+    *out = sms * per_sm;
+    return cudaSuccess;
+}
+
+// Workspace for a gather with up to `n_sources` sources, sized for the most
+// CTAs any mode can launch on the device.
+Layout layout_for(fhd_op op, int64_t N, int64_t M, int sms) {
+    Layout L{};
+    const int64_t max_sources = (op == FHD_OP_FHD) ? M : (op == FHD_OP_FWD) ? N : std::max(N, M);
+    const int64_t padded = ceil_div(std::max<int64_t>(max_sources, 1), kTile) * kTile;
+    const int64_t ctas = (int64_t)sms * kMinCtasPerSm;
+    size_t off = kHeaderBytes;
+    L.packed = off;
+    off = align_up(off + (size_t)padded * kRecordBytes, kWsAlign);
+    L.partial = off;
+    off = align_up(off + (size_t)(2 * ctas) * 2 * kTargetsPerBlock * sizeof(float), kWsAlign);
+    L.frho = off;
+    if (op == FHD_OP_FHF) off = align_up(off + (size_t)2 * std::max<int64_t>(M, 1) * sizeof(float), kWsAlign);
+    L.total = off;
+    return L;
+}
+
+// ---------------------------------------------------------------- validation
+typedef CUresult(CUDAAPI* PFN_range)(CUdeviceptr*, size_t*, CUdeviceptr);
+
+struct Buf {
+    const void* p;
+    size_t bytes;
+};
+
+bool overlaps(const Buf& a, const Buf& b) {
+    if (a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = (uintptr_t)a.p, b0 = (uintptr_t)b.p;
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// Device-memory, alignment and allocation-range checks for one array.
+fhd_status check_array(const void* p, size_t bytes, size_t align, int device) {
+    if (bytes == 0) return FHD_OK;
+    if (p == nullptr) return FHD_ERR_INVALID_VALUE;
+    if ((uintptr_t)p % align != 0) return FHD_ERR_MISALIGNED;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return FHD_ERR_INVALID_VALUE;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return FHD_ERR_INVALID_VALUE;
+    if (attr.type == cudaMemoryTypeDevice && attr.device != device) return FHD_ERR_INVALID_VALUE;
+    // Driver entry point, resolved once per process (thread-safe static init).
+    static const PFN_range range_fn = [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const bool ok = cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 12000, cudaEnableDefault,
+                                                         &q) == cudaSuccess &&
+                        q == cudaDriverEntryPointSuccess;
+        cudaGetLastError();
+        return ok ? (PFN_range)fn : (PFN_range) nullptr;
+    }();
+    if (range_fn) {
+        CUdeviceptr base = 0;
+        size_t size = 0;
+        if (range_fn(&base, &size, (CUdeviceptr)(uintptr_t)p) == CUDA_SUCCESS) {
+            if ((uintptr_t)p + bytes > (uintptr_t)base + size) return FHD_ERR_RANGE;
+        }
+    }
+    return FHD_OK;
+}
+
+fhd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FHD_OK : FHD_ERR_CUDA; }
+
+// ---------------------------------------------------------------- launches
+struct GatherProblem {
+    // targets
+    int64_t n_targets;
+    const float *tx, *ty, *tz;
+    // sources
+    int64_t n_sources;
+    const float *sx, *sy, *sz, *wr, *wi;
+    float sign;  // +1: adjoint kernel; -1: forward (source coordinates negated)
+    // outputs
+    float *out_r, *out_i;
+};
+
+fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, const Layout& L, int device,
+                      cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop, int64_t skip_tile,
+                      bool first_pass = true) {
+    if (g.n_targets == 0) return FHD_OK;
+    if (g.n_sources == 0) {
+        cudaError_t e = first_pass ? cudaMemsetAsync(ws, 0, sizeof(uint32_t), stream) : cudaSuccess;
+        if (e == cudaSuccess) e = cudaMemsetAsync(g.out_r, 0, (size_t)g.n_targets * sizeof(float), stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(g.out_i, 0, (size_t)g.n_targets * sizeof(float), stream);
+        return cuda_status(e);
+    }
+    int ctas_max = 0;
+    cudaError_t e = max_ctas(device, mode, &ctas_max);
+    if (e != cudaSuccess) return FHD_ERR_CUDA;
+
+    Schedule sch;
+    sch.n_targets = g.n_targets;
+    sch.n_tiles = ceil_div(g.n_sources, kTile);
+    sch.n_blocks = ceil_div(g.n_targets, kTargetsPerBlock);
+    sch.work = sch.n_blocks * sch.n_tiles;
+    sch.ctas = (int)std::min<int64_t>(ctas_max, sch.work);
+
+    uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+    float4* packed = reinterpret_cast<float4*>(ws + L.packed);
+    float* partial = reinterpret_cast<float*>(ws + L.partial);
+
+    const int64_t padded = sch.n_tiles * kTile;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    const int pack_grid = (int)std::min<int64_t>(ceil_div(padded, 256), (int64_t)sms * 8);
+    pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, g.sign, g.n_sources, padded,
+                                                packed, status, first_pass ? 1 : 0);
+    if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
+
+    GatherArgs a;
+    a.sch = sch;
+    a.tx = g.tx;
+    a.ty = g.ty;
+    a.tz = g.tz;
+    a.packed = packed;
+    a.out_r = g.out_r;
+    a.out_i = g.out_i;
+    a.partial = partial;
+    a.status = status;
+    a.wait_limit_ns = kWaitLimitNs;
+    a.skip_tile = skip_tile;
+
+    if (ev_start && (e = cudaEventRecord(ev_start, stream)) != cudaSuccess) return FHD_ERR_CUDA;
+    const size_t smem = sizeof(GatherSmem);
+    if (mode == FHD_MODE_FAST) {
+        cudaFuncSetAttribute(gather_kernel<kFast>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        gather_kernel<kFast><<<sch.ctas, kCtaThreads, smem, stream>>>(a);
+    } else {
+        cudaFuncSetAttribute(gather_kernel<kAccurate>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        gather_kernel<kAccurate><<<sch.ctas, kCtaThreads, smem, stream>>>(a);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
+    if (sch.ctas > 1) {
+        fixup_kernel<<<sch.ctas - 1, 256, 0, stream>>>(sch, partial, g.out_r, g.out_i);
+        if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
+    }
+    if (ev_stop && (e = cudaEventRecord(ev_stop, stream)) != cudaSuccess) return FHD_ERR_CUDA;
+    return FHD_OK;
+}
+
+bool valid_mode(fhd_mode m) { return m == FHD_MODE_ACCURATE || m == FHD_MODE_FAST; }
+
+// Shared validation for the three operators.  `ins`/`outs` list every array.
+fhd_status validate(fhd_op op, int64_t N, int64_t M, fhd_mode mode, const Buf* ins, int n_in, const Buf* outs,
+                    int n_out, void* workspace, size_t workspace_bytes, int* device_out, Layout* L) {
+    if (N < 0 || M < 0 || !valid_mode(mode)) return FHD_ERR_INVALID_VALUE;
+    // int64 index arithmetic in the kernels stays far from overflow below 2^40 elements
+    if (N > (int64_t(1) << 40) || M > (int64_t(1) << 40)) return FHD_ERR_INVALID_VALUE;
+    // NULL checks first: they need no CUDA call
+    for (int i = 0; i < n_in; ++i)
+        if (ins[i].bytes && !ins[i].p) return FHD_ERR_INVALID_VALUE;
+    for (int i = 0; i < n_out; ++i)
+        if (outs[i].bytes && !outs[i].p) return FHD_ERR_INVALID_VALUE;
+    for (int i = 0; i < n_in; ++i)
+        if (ins[i].bytes && (uintptr_t)ins[i].p % 4) return FHD_ERR_MISALIGNED;
+    for (int i = 0; i < n_out; ++i)
+        if (outs[i].bytes && (uintptr_t)outs[i].p % 4) return FHD_ERR_MISALIGNED;
+    const bool has_work = [&] {
+        for (int i = 0; i < n_out; ++i)
+            if (outs[i].bytes) return true;
+        return false;
+    }();
+    if (has_work) {
+        if (!workspace) return FHD_ERR_WORKSPACE;
+        if ((uintptr_t)workspace % kWsAlign) return FHD_ERR_MISALIGNED;
+    }
+    for (int i = 0; i < n_out; ++i) {
+        for (int j = 0; j < n_in; ++j)
+            if (overlaps(outs[i], ins[j])) return FHD_ERR_ALIAS;
+        for (int j = i + 1; j < n_out; ++j)
+            if (overlaps(outs[i], outs[j])) return FHD_ERR_ALIAS;
+    }
+    if (!has_work) {
+        *device_out = -1;
+        return FHD_OK;
+    }
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) {
+        cudaGetLastError();
+        return FHD_ERR_CUDA;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        cudaGetLastError();
+        return FHD_ERR_CUDA;
+    }
+    *L = layout_for(op, N, M, sms);
+    if (workspace_bytes < L->total) return FHD_ERR_WORKSPACE;
+    const Buf wsb{workspace, L->total};
+    for (int i = 0; i < n_out; ++i)
+        if (overlaps(outs[i], wsb)) return FHD_ERR_ALIAS;
+    for (int i = 0; i < n_in; ++i)
+        if (overlaps(ins[i], wsb)) return FHD_ERR_ALIAS;
+    fhd_status s;
+    for (int i = 0; i < n_in; ++i)
+        if ((s = check_array(ins[i].p, ins[i].bytes, 4, device)) != FHD_OK) return s;
+    for (int i = 0; i < n_out; ++i)
+        if ((s = check_array(outs[i].p, outs[i].bytes, 4, device)) != FHD_OK) return s;
+    if ((s = check_array(workspace, L->total, kWsAlign, device)) != FHD_OK) return s;
+    *device_out = device;
+    return FHD_OK;
+}
+
+fhd_status fhd_compute_impl(int64_t M, const float* kx, const float* ky, const float* kz, const float* Dr,
+                            const float* Di, int64_t N, const float* x, const float* y, const float* z,
+                            float* rho_r, float* rho_i, fhd_mode mode, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1, int64_t skip_tile) {
+    const size_t mb = (size_t)(N > 0 ? M : 0) * 4, nb = (size_t)N * 4;
+    const Buf ins[] = {{kx, mb}, {ky, mb}, {kz, mb}, {Dr, mb}, {Di, mb}, {x, nb}, {y, nb}, {z, nb}};
+    const Buf outs[] = {{rho_r, nb}, {rho_i, nb}};
+    int device = -1;
+    Layout L;
+    fhd_status s = validate(FHD_OP_FHD, N, M, mode, ins, 8, outs, 2, workspace, workspace_bytes, &device, &L);
+    if (s != FHD_OK || device < 0) return s;
+    GatherProblem g{N, x, y, z, M, kx, ky, kz, Dr, Di, 1.0f, rho_r, rho_i};
+    return run_gather(g, mode, (unsigned char*)workspace, L, device, stream, ev0, ev1, skip_tile);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fhd_workspace_bytes(fhd_op op, int64_t N, int64_t M, int device) {
+    if (N < 0 || M < 0) return 0;
+    if (op != FHD_OP_FHD && op != FHD_OP_FWD && op != FHD_OP_FHF) return 0;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return layout_for(op, N, M, sms).total;
+}
+
+fhd_status fhd_compute(int64_t M, const float* kx, const float* ky, const float* kz, const float* Dr,
+                       const float* Di, int64_t N, const float* x, const float* y, const float* z, float* rho_r,
+                       float* rho_i, fhd_mode mode, void* workspace, size_t workspace_bytes, fhd_stream_t stream) {
+    return fhd_compute_impl(M, kx, ky, kz, Dr, Di, N, x, y, z, rho_r, rho_i, mode, workspace, workspace_bytes,
+                            (cudaStream_t)stream, nullptr, nullptr, -1);
+}
+
+fhd_status fhd_compute_profiled(int64_t M, const float* kx, const float* ky, const float* kz, const float* Dr,
+                                const float* Di, int64_t N, const float* x, const float* y, const float* z,
+                                float* rho_r, float* rho_i, fhd_mode mode, void* workspace,
+                                size_t workspace_bytes, fhd_stream_t stream, fhd_event_t gather_start,
+                                fhd_event_t gather_stop) {
+    return fhd_compute_impl(M, kx, ky, kz, Dr, Di, N, x, y, z, rho_r, rho_i, mode, workspace, workspace_bytes,
+                            (cudaStream_t)stream, (cudaEvent_t)gather_start, (cudaEvent_t)gather_stop, -1);
+}
+
+fhd_status fwd_compute(int64_t N, const float* x, const float* y, const float* z, const float* rho_r,
+                       const float* rho_i, int64_t M, const float* kx, const float* ky, const float* kz, float* Dr,
+                       float* Di, fhd_mode mode, void* workspace, size_t workspace_bytes, fhd_stream_t stream) {
+    const size_t nb = (size_t)(M > 0 ? N : 0) * 4, mb = (size_t)M * 4;
+    const Buf ins[] = {{x, nb}, {y, nb}, {z, nb}, {rho_r, nb}, {rho_i, nb}, {kx, mb}, {ky, mb}, {kz, mb}};
+    const Buf outs[] = {{Dr, mb}, {Di, mb}};
+    int device = -1;
+    Layout L;
+    fhd_status s = validate(FHD_OP_FWD, N, M, mode, ins, 8, outs, 2, workspace, workspace_bytes, &device, &L);
+    if (s != FHD_OK || device < 0) return s;
+    GatherProblem g{M, kx, ky, kz, N, x, y, z, rho_r, rho_i, -1.0f, Dr, Di};
+    return run_gather(g, mode, (unsigned char*)workspace, L, device, (cudaStream_t)stream, nullptr, nullptr, -1);
+}
+
+fhd_status fhfrho_apply(int64_t N, const float* x, const float* y, const float* z, const float* rho_r,
+                        const float* rho_i, int64_t M, const float* kx, const float* ky, const float* kz,
+                        float* out_r, float* out_i, fhd_mode mode, void* workspace, size_t workspace_bytes,
+                        fhd_stream_t stream) {
+    const size_t nb = (size_t)N * 4, mb = (size_t)(N > 0 ? M : 0) * 4;
+    const Buf ins[] = {{x, nb}, {y, nb}, {z, nb}, {rho_r, nb}, {rho_i, nb}, {kx, mb}, {ky, mb}, {kz, mb}};
+    const Buf outs[] = {{out_r, nb}, {out_i, nb}};
+    int device = -1;
+    Layout L;
+    fhd_status s = validate(FHD_OP_FHF, N, M, mode, ins, 8, outs, 2, workspace, workspace_bytes, &device, &L);
+    if (s != FHD_OK || device < 0) return s;
+    unsigned char* ws = (unsigned char*)workspace;
+    if (M == 0) {
+        cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), (cudaStream_t)stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(out_r, 0, nb, (cudaStream_t)stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(out_i, 0, nb, (cudaStream_t)stream);
+        return cuda_status(e);
+    }
+    float* fr = reinterpret_cast<float*>(ws + L.frho);
+    float* fi = fr + M;
+    // pass 1: F rho, gathered per sample (voxels are the sources, coordinates negated)
+    GatherProblem g1{M, kx, ky, kz, N, x, y, z, rho_r, rho_i, -1.0f, fr, fi};
+    s = run_gather(g1, mode, ws, L, device, (cudaStream_t)stream, nullptr, nullptr, -1);
+    if (s != FHD_OK) return s;
+    // pass 2: F^H (F rho), gathered per voxel
+    GatherProblem g2{N, x, y, z, M, kx, ky, kz, fr, fi, 1.0f, out_r, out_i};
+    return run_gather(g2, mode, ws, L, device, (cudaStream_t)stream, nullptr, nullptr, -1, false);
+}
+
+fhd_status fhd_workspace_status(const void* workspace, fhd_stream_t stream) {
+    if (!workspace) return FHD_ERR_INVALID_VALUE;
+    uint32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return FHD_ERR_CUDA;
+    return word == 0 ? FHD_OK : FHD_ERR_TIMEOUT;
+}
+
+const char* fhd_status_string(fhd_status s) {
+    switch (s) {
+        case FHD_OK: return "ok";
+        case FHD_ERR_INVALID_VALUE: return "invalid value (size, NULL pointer, mode, op or non-device memory)";
+        case FHD_ERR_MISALIGNED: return "misaligned pointer (arrays need 4 bytes, workspace 256 bytes)";
+        case FHD_ERR_ALIAS: return "an output overlaps an input, another output or the workspace";
+        case FHD_ERR_WORKSPACE: return "workspace smaller than fhd_workspace_bytes()";
+        case FHD_ERR_CUDA: return "CUDA runtime error";
+        case FHD_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+        case FHD_ERR_RANGE: return "array extends past the end of its device allocation";
+    }
+    return "unknown status";
+}
+
+fhd_status fhd_launch_shape(int device, fhd_mode mode, int* ctas, int* threads, int* targets_per_thread,
+                            int* tile_sources, int* stages) {
+    if (!valid_mode(mode)) return FHD_ERR_INVALID_VALUE;
+    int n = 0;
+    if (max_ctas(device, mode, &n) != cudaSuccess) {
+        cudaGetLastError();
+        return FHD_ERR_INVALID_VALUE;
+    }
+    if (ctas) *ctas = n;
+    if (threads) *threads = kThreads;
+    if (targets_per_thread) *targets_per_thread = kV;
+    if (tile_sources) *tile_sources = kTile;
+    if (stages) *stages = kStages;
+    return FHD_OK;
+}
+
+int fhd_version(void) { return kVersion; }
+
+// Declared in include/fhd_testing.h.
+fhd_status fhd_test_check_array(const void* p, size_t bytes, int device) {
+    if (bytes == 0) return p ? check_array(p, 4, 4, device) : FHD_ERR_INVALID_VALUE;
+    return check_array(p, bytes, 4, device);
+}
+
+// Declared in include/fhd_testing.h.  Replays, on the host, the segment
+// logic of gather_kernel and fixup_kernel over the Schedule methods they use.
+int fhd_test_schedule(int64_t n_targets, int64_t n_sources, int ctas) {
+    if (n_targets <= 0 || n_sources <= 0 || ctas <= 0) return 1;
+    Schedule sch;
+    sch.n_targets = n_targets;
+    sch.n_tiles = ceil_div(n_sources, kTile);
+    sch.n_blocks = ceil_div(n_targets, kTargetsPerBlock);
+    sch.work = sch.n_blocks * sch.n_tiles;
+    sch.ctas = (int)std::min<int64_t>(ctas, sch.work);
+    if (sch.start(0) != 0 || sch.start(sch.ctas) != sch.work) return 2;
+    std::vector<int> direct(sch.n_blocks, 0), fixed(sch.n_blocks, 0);
+    // (cta, block) -> [first tile, last tile] of the partial segment in that slot
+    std::vector<int64_t> slot_block(2 * (size_t)sch.ctas, -1), slot_lo(2 * (size_t)sch.ctas, -1),
+        slot_hi(2 * (size_t)sch.ctas, -1);
+    for (int64_t c = 0; c < sch.ctas; ++c) {
+        const int64_t w0 = sch.start(c), w1 = sch.start(c + 1);
+        if (w1 <= w0) return 3;  // every CTA owns at least one item
+        int64_t seg_first = 0;
+        for (int64_t w = w0; w < w1; ++w) {
+            const int64_t b = w / sch.n_tiles, j = w % sch.n_tiles;
+            if (w == w0 || j == 0) seg_first = j;
+            if (w == w1 - 1 || j == sch.n_tiles - 1) {
+                if (seg_first == 0 && j == sch.n_tiles - 1) {
+                    direct[b]++;
+                } else {
+                    const int64_t sl = sch.slot(c, b);
+                    if (sl < 2 * c || sl > 2 * c + 1) return 4;
+                    if (slot_block[sl] != -1) return 5;  // slot written twice
+                    slot_block[sl] = b;
+                    slot_lo[sl] = seg_first;
+                    slot_hi[sl] = j;
+                }
+            }
+        }
+    }
+    for (int64_t c = 1; c < sch.ctas; ++c) {
+        const int64_t b = sch.fixup_block(c);
+        if (b < 0) continue;
+        fixed[b]++;
+        const int64_t hi = sch.last_contributor(c, b);
+        int64_t next = 0;  // contributors' tile ranges must tile [0, n_tiles) in order
+        for (int64_t cc = c - 1; cc <= hi; ++cc) {
+            const int64_t sl = sch.slot(cc, b);
+            if (slot_block[sl] != b) return 6;
+            if (slot_lo[sl] != next) return 7;
+            next = slot_hi[sl] + 1;
+        }
+        if (next != sch.n_tiles) return 8;
+    }
+    for (int64_t b = 0; b < sch.n_blocks; ++b)
+        if (direct[b] + fixed[b] != 1) return 9;  // every block finished exactly once
+    return 0;
+}
+
+fhd_status fhd_test_compute_skip_tile(int64_t M, const float* kx, const float* ky, const float* kz,
+                                      const float* Dr, const float* Di, int64_t N, const float* x, const float* y,
+                                      const float* z, float* rho_r, float* rho_i, fhd_mode mode, void* workspace,
+                                      size_t workspace_bytes, fhd_stream_t stream, int64_t skip_tile) {
+    return fhd_compute_impl(M, kx, ky, kz, Dr, Di, N, x, y, z, rho_r, rho_i, mode, workspace, workspace_bytes,
+                            (cudaStream_t)stream, nullptr, nullptr, skip_tile);
+}
+
+}  // extern "C"

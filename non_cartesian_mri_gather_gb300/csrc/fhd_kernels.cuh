@@ -1,0 +1,394 @@
+// fhd_kernels.cuh - sm_103a kernels for the non-uniform Fourier sums.
+//
+// One gather kernel serves both directions.  For the adjoint F^H D
+// ("Case study - iterative MRI reconstruction", section 17.3, rho_n equation)
+// the targets are voxels and the sources are samples {k, D}:
+//
+//     out_t = sum_s w_s exp(+i 2 pi (a_s . b_t))
+//
+// with b_t = x_n, a_s = k_m, w_s = D_m.  The forward sum F rho has the kernel
+// exp(-i 2 pi k.x) = exp(+i 2 pi k.(-x)), so it is the same gather with the
+// samples as targets and the voxels, coordinates negated (exact in fp32), as
+// sources.  That is the loop fission of section 17.3.2: F^H F rho runs as a
+// forward gather followed by an adjoint gather, each its own kernel.
+//
+// Pipeline of one call:
+//   1. pack_sources   - loop fission / per-source precompute (section 17.3.2):
+//                       SoA source arrays -> 32-byte AoS records
+//                       {a.x, a.y, a.z, w.re, w.im, 0, 0, 0}, padded with
+//                       zero-weight records to a whole number of tiles.  The
+//                       array-of-structures record follows the mtuann notes'
+//                       step 4 and the SampleChunk struct of section 17.3.4.
+//   2. gather_kernel  - persistent CTAs; each owns an equal contiguous range
+//                       of (target block, source tile) work items.  A
+//                       producer warp streams source tiles into a shared-
+//                       memory ring with non-multicast bulk async copies
+//                       completing on mbarriers; consumer warps read each
+//                       record as a broadcast (the role the constant cache
+//                       plays in section 17.3.4), keep V targets' coordinates
+//                       and accumulators in registers (privatisation, section
+//                       17.3.3) and write every output once.
+//   3. fixup_kernel   - target blocks whose source range was split between
+//                       CTAs are summed from per-CTA partials in a fixed
+//                       order (no atomics, bit-reproducible).
+//
+// Every pipeline wait is bounded by a time limit; on expiry the waiting
+// thread records an error bit in the status word and its CTA leaves early
+// after the producer has drained its own copies in flight.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fhd {
+
+// ---------------------------------------------------------------- shape
+constexpr int kThreads = 256;            // consumer threads per CTA
+constexpr int kWarps = kThreads / 32;    // consumer warps
+constexpr int kV = 8;                    // targets per consumer thread
+constexpr int kTargetsPerBlock = kThreads * kV;
+constexpr int kTile = 128;               // sources per staged tile
+constexpr int kStages = 4;               // shared-memory ring depth
+constexpr int kRecordBytes = 32;         // one packed source
+constexpr int kTileBytes = kTile * kRecordBytes;
+constexpr int kCtaThreads = kThreads + 32;  // + one producer warp
+constexpr int kMinCtasPerSm = 2;
+
+// status word bits
+constexpr uint32_t kStatusConsumerTimeout = 1u;
+constexpr uint32_t kStatusProducerTimeout = 2u;
+constexpr uint32_t kStatusDrainTimeout = 4u;
+
+enum Mode : int { kAccurate = 0, kFast = 1 };
+
+// Static schedule shared by the gather and fix-up kernels (and by the
+// host-side schedule check).  The work items (target block b, source tile j)
+// are numbered w = b * n_tiles + j and CTA c owns [start(c), start(c+1)).
+// The part of CTA c's range inside block b is a "segment"; a segment that
+// covers all of block b's tiles is written straight to the output, any other
+// segment goes to a partial slot of CTA c: slot 2c for its first block, 2c+1
+// for its last (only the first and the last segment of a range can be
+// partial).  A block is split exactly when some boundary start(c), c >= 1,
+// lies strictly inside it; the lowest such boundary owns the block's fix-up,
+// whose contributors are CTAs c-1 .. last_contributor().
+struct Schedule {
+    int64_t n_targets;   // targets (voxels for F^H D, samples for F rho)
+    int64_t n_tiles;     // source tiles per target block
+    int64_t n_blocks;    // target blocks of kTargetsPerBlock
+    int64_t work;        // n_blocks * n_tiles
+    int ctas;            // persistent CTAs in the launch
+
+    __host__ __device__ int64_t start(int64_t c) const { return (c * work) / ctas; }
+    __host__ __device__ int64_t first_block(int64_t c) const { return start(c) / n_tiles; }
+    __host__ __device__ int64_t slot(int64_t c, int64_t b) const { return 2 * c + (b == first_block(c) ? 0 : 1); }
+    // Block whose fix-up boundary c (1 <= c < ctas) owns, or -1.
+    __host__ __device__ int64_t fixup_block(int64_t c) const {
+        if (c < 1 || c >= ctas) return -1;
+        const int64_t s = start(c);
+        if (s % n_tiles == 0) return -1;
+        const int64_t b = s / n_tiles;
+        if (c >= 2 && start(c - 1) > b * n_tiles) return -1;  // an earlier boundary owns block b
+        return b;
+    }
+    // Last CTA whose range intersects block b, scanning up from CTA c.
+    __host__ __device__ int64_t last_contributor(int64_t c, int64_t b) const {
+        while (c + 1 < ctas && start(c + 1) < (b + 1) * n_tiles) ++c;
+        return c;
+    }
+};
+
+struct GatherArgs {
+    Schedule sch;
+    const float* __restrict__ tx;   // target coordinates
+    const float* __restrict__ ty;
+    const float* __restrict__ tz;
+    const float4* __restrict__ packed;  // n_tiles * kTile records of 2 float4
+    float* __restrict__ out_r;
+    float* __restrict__ out_i;
+    float* __restrict__ partial;    // [2*ctas slots][2][kTargetsPerBlock]
+    uint32_t* status;
+    uint64_t wait_limit_ns;          // bounded-wait time limit
+    int64_t skip_tile;               // test hook: work item whose copy is never issued (-1: none)
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `bar` with parity `parity` to complete, for at most
+// `limit_ns` (plus an iteration cap in case the timer does not advance).
+// On expiry sets `code` in the status word and returns false.
+__device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                               uint32_t code, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1; it < (1u << 26); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0 && global_timer_ns() - t0 > limit_ns) break;
+    }
+    atomicOr(status, code);
+    return false;
+}
+
+// Bulk async copy global -> this CTA's shared memory, completing on `bar`.
+// Both addresses 16-byte aligned, size a multiple of 16 (kTileBytes is).
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------- per-pair math
+// exp(+i 2 pi p) for the fp32 phase p (cycles): p is reduced by its nearest
+// integer (t = p - rint(p), exact in fp32 for |p| < 2^23), then
+//   accurate: sincospif(2 t)             (sin, cos of 2 pi t)
+//   fast:     __sinf/__cosf(2 pi t)      (hardware approximations)
+template <int MODE>
+__device__ __forceinline__ void unit_phasor(float p, float& s, float& c) {
+    const float t = p - rintf(p);
+    if constexpr (MODE == kAccurate) {
+        sincospif(2.0f * t, &s, &c);
+    } else {
+        const float a = 6.28318530717958647692f * t;
+        s = __sinf(a);
+        c = __cosf(a);
+    }
+}
+
+// ---------------------------------------------------------------- pack
+// Source records {sign*a.x, sign*a.y, sign*a.z, w.re, w.im, 0, 0, 0}.
+// Records n..n_padded-1 are zero (weight 0, so they add exactly 0).
+// With `reset_status`, block 0 thread 0 also clears the status word (stream
+// order puts this before the gather kernel); the second pass of F^H F rho
+// keeps the word so a timeout of the first pass stays visible.
+__global__ void pack_sources(const float* __restrict__ ax, const float* __restrict__ ay,
+                             const float* __restrict__ az, const float* __restrict__ wr,
+                             const float* __restrict__ wi, float sign, int64_t n, int64_t n_padded,
+                             float4* __restrict__ out, uint32_t* status, int reset_status) {
+    if (reset_status && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_padded;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 r1 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < n) {
+            r0 = make_float4(sign * ax[i], sign * ay[i], sign * az[i], wr[i]);
+            r1.x = wi[i];
+        }
+        out[2 * i] = r0;
+        out[2 * i + 1] = r1;
+    }
+}
+
+// ---------------------------------------------------------------- gather
+struct __align__(16) GatherSmem {
+    float4 ring[kStages][kTile * 2];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(const GatherArgs args) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    GatherSmem& sm = *reinterpret_cast<GatherSmem*>(smem_raw);
+
+    const Schedule& sch = args.sch;
+    const int c = blockIdx.x;
+    const int64_t w_begin = sch.start(c);
+    const int64_t w_end = sch.start(c + 1);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kStages; ++st) {
+            mbar_init(&sm.full[st], 1);
+            mbar_init(&sm.empty[st], kWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();  // the only CTA-wide barrier: before any bounded wait
+
+    if (warp == kWarps) {
+        // ------------------------------------------------ producer warp
+        if (lane != 0) return;
+        int64_t issued = 0;
+        bool ok = true;
+        for (int64_t w = w_begin; w < w_end && ok; ++w, ++issued) {
+            const int st = (int)(issued % kStages);
+            if (issued >= kStages) {
+                const uint32_t par = (uint32_t)(((issued / kStages) - 1) & 1);
+                ok = mbar_wait_bounded(&sm.empty[st], par, args.status, kStatusProducerTimeout,
+                                       args.wait_limit_ns);
+                if (!ok) break;
+            }
+            if (w == args.skip_tile) continue;  // test hook: this copy never arrives
+            const int64_t j = w % sch.n_tiles;
+            mbar_arrive_expect_tx(&sm.full[st], kTileBytes);
+            bulk_copy_g2s(&sm.ring[st][0], args.packed + j * (kTile * 2), kTileBytes, &sm.full[st]);
+        }
+        // Drain: the last copy issued into each stage must have landed before
+        // this CTA's shared memory can be released.
+        for (int st = 0; st < kStages; ++st) {
+            // last index < issued that maps to stage st
+            if (issued <= st) continue;
+            const int64_t last = st + ((issued - 1 - st) / kStages) * kStages;
+            if (w_begin + last == args.skip_tile) continue;
+            mbar_wait_bounded(&sm.full[st], (uint32_t)((last / kStages) & 1), args.status, kStatusDrainTimeout,
+                              args.wait_limit_ns);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps
+    float bx[kV], by[kV], bz[kV];
+    float acc_r[kV], acc_i[kV];
+    int64_t seg_first_tile = 0;  // first tile index of the current segment
+    int64_t consumed = 0;
+
+    for (int64_t w = w_begin; w < w_end; ++w, ++consumed) {
+        const int64_t b = w / sch.n_tiles;
+        const int64_t j = w % sch.n_tiles;
+        if (w == w_begin || j == 0) {
+            // new segment: this CTA's range enters target block b
+            seg_first_tile = j;
+            const int64_t base = b * kTargetsPerBlock + threadIdx.x;
+#pragma unroll
+            for (int v = 0; v < kV; ++v) {
+                const int64_t t = base + (int64_t)v * kThreads;
+                const bool in = t < sch.n_targets;
+                bx[v] = in ? args.tx[t] : 0.f;
+                by[v] = in ? args.ty[t] : 0.f;
+                bz[v] = in ? args.tz[t] : 0.f;
+                acc_r[v] = 0.f;
+                acc_i[v] = 0.f;
+            }
+        }
+
+        const int st = (int)(consumed % kStages);
+        if (!mbar_wait_bounded(&sm.full[st], (uint32_t)((consumed / kStages) & 1), args.status,
+                               kStatusConsumerTimeout, args.wait_limit_ns))
+            return;
+
+        // Two-level accumulation: a fresh accumulator per tile, folded into the
+        // running sum once per tile, keeps fp32 rounding growth at
+        // O(sqrt(kTile) + sqrt(M / kTile)) instead of O(sqrt(M)).
+        float tr[kV], ti[kV];
+#pragma unroll
+        for (int v = 0; v < kV; ++v) {
+            tr[v] = 0.f;
+            ti[v] = 0.f;
+        }
+        const float4* rec = &sm.ring[st][0];
+#pragma unroll 2
+        for (int s = 0; s < kTile; ++s) {
+            const float4 a = rec[2 * s];                                         // a.x a.y a.z w.re
+            const float wim = reinterpret_cast<const float*>(rec)[8 * s + 4];   // w.im
+#pragma unroll
+            for (int v = 0; v < kV; ++v) {
+                const float p = fmaf(a.z, bz[v], fmaf(a.y, by[v], a.x * bx[v]));
+                float sn, cs;
+                unit_phasor<MODE>(p, sn, cs);
+                tr[v] = fmaf(a.w, cs, tr[v]);
+                tr[v] = fmaf(-wim, sn, tr[v]);
+                ti[v] = fmaf(a.w, sn, ti[v]);
+                ti[v] = fmaf(wim, cs, ti[v]);
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < kV; ++v) {
+            acc_r[v] += tr[v];
+            acc_i[v] += ti[v];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[st]);
+
+        if (w == w_end - 1 || j == sch.n_tiles - 1) {
+            // end of segment: whole block -> output, else -> this CTA's partial slot
+            const bool whole = (seg_first_tile == 0) && (j == sch.n_tiles - 1);
+            const int64_t base = b * kTargetsPerBlock + threadIdx.x;
+            if (whole) {
+#pragma unroll
+                for (int v = 0; v < kV; ++v) {
+                    const int64_t t = base + (int64_t)v * kThreads;
+                    if (t < sch.n_targets) {
+                        args.out_r[t] = acc_r[v];
+                        args.out_i[t] = acc_i[v];
+                    }
+                }
+            } else {
+                const int64_t slot = sch.slot(c, b);
+                float* pr = args.partial + slot * (2 * kTargetsPerBlock);
+                float* pi = pr + kTargetsPerBlock;
+#pragma unroll
+                for (int v = 0; v < kV; ++v) {
+                    pr[threadIdx.x + v * kThreads] = acc_r[v];
+                    pi[threadIdx.x + v * kThreads] = acc_i[v];
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- fix-up
+// One CTA per CTA boundary c = 1..ctas-1.  A boundary strictly inside target
+// block b means b was split; the lowest such boundary sums b's partial slots
+// over the contributing CTAs c-1 .. c_hi in increasing order.
+__global__ void fixup_kernel(const Schedule sch, const float* __restrict__ partial, float* __restrict__ out_r,
+                             float* __restrict__ out_i) {
+    const int64_t c = (int64_t)blockIdx.x + 1;
+    const int64_t b = sch.fixup_block(c);
+    if (b < 0) return;
+    const int64_t c_lo = c - 1;
+    const int64_t c_hi = sch.last_contributor(c, b);
+    for (int l = threadIdx.x; l < kTargetsPerBlock; l += blockDim.x) {
+        const int64_t t = b * kTargetsPerBlock + l;
+        if (t >= sch.n_targets) break;
+        float sr = 0.f, si = 0.f;
+        for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
+            const float* pr = partial + sch.slot(cc, b) * (2 * kTargetsPerBlock);
+            sr += pr[l];
+            si += pr[kTargetsPerBlock + l];
+        }
+        out_r[t] = sr;
+        out_i[t] = si;
+    }
+}
+
+}  // namespace fhd

@@ -1,0 +1,203 @@
+"""GPU parity: the CUDA library against the fp64 oracle, element by element.
+
+Small problems are compared on every output; they span several target blocks
+(2048 targets) and source tiles (128 sources) with ragged tails.  The five
+benchmark workloads run at full size in the launch configuration the
+benchmark uses; workloads 1-2 are compared on every voxel, workloads 3-4 on a
+fixed spread of sampled voxels (a gather output depends only on its own voxel,
+so a sampled output is exact for that voxel), and workload 5 through its two
+passes plus properties that hold at any size.
+
+Tolerances: relative L2 error <= 1e-5 (accurate mode) and <= 1e-3 with
+PSNR >= 60 dB (fast mode).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from inputs import make_workload, random_problem
+from tests.gpu_helpers import (PSNR_FAST_DB, TOL_ACCURATE, TOL_FAST, gpu_fhd, gpu_fhf, gpu_fwd, psnr_db, rel_l2,
+                               sample_indices)
+
+pytestmark = pytest.mark.gpu
+
+ACC, FAST = 0, 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from non_cartesian_mri_gather_gb300 import build, load
+
+    build.build()
+    load()
+    torch.cuda.set_device(0)
+
+
+def check(got, ref, mode, what):
+    err = rel_l2(got, ref)
+    if mode == ACC:
+        assert err <= TOL_ACCURATE, f"{what}: accurate relL2 {err:.3e}"
+    else:
+        assert err <= TOL_FAST, f"{what}: fast relL2 {err:.3e}"
+        assert psnr_db(got, ref) >= PSNR_FAST_DB, f"{what}: fast PSNR {psnr_db(got, ref):.1f} dB"
+    return err
+
+
+# ------------------------------------------------------------ small, every output
+
+SIZES = [(1, 1), (31, 127), (1000, 129), (2049, 1000), (5000, 3001), (20000, 777), (100, 40000), (4096, 256)]
+
+
+@pytest.mark.parametrize("N,M", SIZES)
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_fhd_random(N, M, mode):
+    p = random_problem(N, M, kmax=32.0, seed=N + 7 * M)
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    check(gpu_fhd(p, mode), ref, mode, f"F^H D N={N} M={M}")
+
+
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_fhd_2d_grid(mode):
+    p = random_problem(4500, 1500, kmax=16.0, seed=3, dims=2, coords="grid")
+    assert np.all(p.z == 0)
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    check(gpu_fhd(p, mode), ref, mode, "F^H D 2D")
+
+
+@pytest.mark.parametrize("N,M", [(1, 1), (127, 31), (3001, 5000), (777, 20000), (40000, 100)])
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_fwd_random(N, M, mode):
+    p = random_problem(N, M, kmax=32.0, seed=N + 5 * M, op="fwd")
+    ref = oracle.forward(p.x, p.y, p.z, p.rho_r + 1j * p.rho_i, p.kx, p.ky, p.kz)
+    check(gpu_fwd(p, mode), ref, mode, f"F rho N={N} M={M}")
+
+
+@pytest.mark.parametrize("N,M", [(1, 1), (2500, 700), (4099, 1333)])
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_fhf_random(N, M, mode):
+    p = random_problem(N, M, kmax=20.0, seed=N + 3 * M, op="fhf")
+    ref = oracle.normal(p.x, p.y, p.z, p.rho_r + 1j * p.rho_i, p.kx, p.ky, p.kz)
+    check(gpu_fhf(p, mode), ref, mode, f"F^H F rho N={N} M={M}")
+
+
+# ------------------------------------------------------------ benchmark workloads
+
+_cache = {}
+
+
+def workload(i):
+    if i not in _cache:
+        _cache[i] = make_workload(i)
+    return _cache[i]
+
+
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_workload1_full(mode):
+    p = workload(1)
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    check(gpu_fhd(p, mode), ref, mode, "workload 1")
+
+
+@pytest.fixture(scope="module")
+def ref2():
+    p = workload(2)
+    return oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+
+
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_workload2_full(mode, ref2):
+    check(gpu_fhd(workload(2), mode), ref2, mode, "workload 2")
+
+
+@pytest.mark.parametrize("wl", [3, 4])
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_workload_sampled(wl, mode):
+    p = workload(wl)
+    got = gpu_fhd(p, mode)
+    idx = sample_indices(p.N, 4096)
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x[idx], p.y[idx], p.z[idx])
+    check(got[idx], ref, mode, f"workload {wl} ({idx.size} sampled voxels)")
+
+
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_workload5(mode):
+    """F^H F rho at 128^3 x 262144: forward pass on sampled samples vs the oracle,
+    the composed operator equal to fhd_compute(fwd_compute(rho)) bit for bit,
+    and <rho, F^H F rho> = ||F rho||^2 (real, positive)."""
+    import torch
+
+    import non_cartesian_mri_gather_gb300 as fhd
+    from tests.gpu_helpers import dev, host_complex
+
+    p = workload(5)
+    t = {k: dev(getattr(p, k)) for k in ("x", "y", "z", "kx", "ky", "kz", "rho_r", "rho_i")}
+    Dr, Di = fhd.fwd_compute(t["x"], t["y"], t["z"], t["rho_r"], t["rho_i"], t["kx"], t["ky"], t["kz"], mode=mode)
+    o_r, o_i = fhd.fhfrho_apply(t["x"], t["y"], t["z"], t["rho_r"], t["rho_i"], t["kx"], t["ky"], t["kz"], mode=mode)
+    c_r, c_i = fhd.fhd_compute(t["kx"], t["ky"], t["kz"], Dr, Di, t["x"], t["y"], t["z"], mode=mode)
+    torch.cuda.synchronize()
+    assert torch.equal(o_r, c_r) and torch.equal(o_i, c_i)
+    Frho = host_complex(Dr, Di)
+    idx = sample_indices(p.M, 512)
+    rho = p.rho_r + 1j * p.rho_i
+    ref = oracle.forward(p.x, p.y, p.z, rho, p.kx[idx], p.ky[idx], p.kz[idx])
+    check(Frho[idx], ref, mode, "workload 5 forward pass (sampled samples)")
+    out = host_complex(o_r, o_i)
+    q = np.vdot(rho.astype(np.complex128), out)
+    nrm = np.vdot(Frho, Frho).real
+    assert abs(q.imag) <= 1e-4 * abs(q.real)
+    assert abs(q.real - nrm) <= (1e-4 if mode == ACC else 1e-2) * nrm
+
+
+# ------------------------------------------------------------ edge cases
+
+def test_empty_and_zero_sources():
+    import torch
+
+    import non_cartesian_mri_gather_gb300 as fhd
+
+    d = "cuda"
+    x = torch.rand(300, device=d) - 0.5
+    e = torch.empty(0, device=d)
+    rr, ri = fhd.fhd_compute(e, e, e, e, e, x, x.clone(), x.clone())
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(rr) == 0 and torch.count_nonzero(ri) == 0
+    o_r, o_i = fhd.fhd_compute(x[:5], x[:5].clone(), x[:5].clone(), x[:5].clone(), x[:5].clone(), e, e.clone(),
+                               e.clone())
+    assert o_r.numel() == 0
+    Dr, Di = fhd.fwd_compute(e, e, e, e, e, x, x.clone(), x.clone())
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(Dr) == 0 and torch.count_nonzero(Di) == 0
+
+
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_deterministic(mode):
+    p = random_problem(30000, 5000, kmax=32.0, seed=21)
+    a = gpu_fhd(p, mode)
+    b = gpu_fhd(p, mode)
+    assert np.array_equal(a, b)
+
+
+def test_workspace_reuse_and_stream():
+    import torch
+
+    import non_cartesian_mri_gather_gb300 as fhd
+    from tests.gpu_helpers import dev, host_complex
+
+    p = random_problem(9000, 2000, kmax=32.0, seed=4)
+    ws = fhd.Workspace(fhd.OP_FHF, p.N, p.M)
+    t = {k: dev(getattr(p, k)) for k in ("x", "y", "z", "kx", "ky", "kz", "Dr", "Di")}
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        r1 = fhd.fhd_compute(t["kx"], t["ky"], t["kz"], t["Dr"], t["Di"], t["x"], t["y"], t["z"], workspace=ws,
+                             stream=s)
+        r2 = fhd.fhd_compute(t["kx"], t["ky"], t["kz"], t["Dr"], t["Di"], t["x"], t["y"], t["z"], workspace=ws,
+                             stream=s)
+    s.synchronize()
+    assert fhd.fhd_workspace_status(ws, s) == 0
+    a, b = host_complex(*r1), host_complex(*r2)
+    assert np.array_equal(a, b)
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    assert rel_l2(a, ref) <= TOL_ACCURATE
