@@ -1,0 +1,415 @@
+"""Benchmark of the F^H D gather on one GB300 (or N replicas under torchrun).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 1..5] [--mode fast|accurate]
+
+Prints ONE JSON line.  The default workload is the 256^3-voxel, 100000-sample
+kooshball F^H D ("Case study - iterative MRI reconstruction", section 17.3:
+the 256^3 x 100k example), in fast mode.
+
+value      voxel-sample pairs per second over the K timed steps, inputs resident
+           in device memory; a step is one fhd_compute call (sample pack, gather,
+           fix-up).  GFLOP/s = 13 flop/pair x pairs/s / 1e9 (k.x: 3 mul + 2 add;
+           complex multiply-accumulate: 4 mul + 4 add; sin/cos not counted).
+e2e        the same metric through the public API with pinned HOST buffers:
+           every step copies the inputs host->device, runs fhd_compute and
+           copies rho back device->host, all inside the timed region.
+roofline   the gather kernel against the plain-ALU bound
+           SMs x clock x min(FMA lanes / 7, MUFU lanes / 2) pairs/s
+           (7 FMA-pipe and 2 MUFU instructions per pair), with the lane counts
+           128 and 16 per SM per clock and the maximum SM clock; the kernel's
+           duration comes from CUDA events recorded on its stream around the
+           gather and fix-up launches of every timed step.
+cpu_baseline  the fp64 CPU oracle on a bounded voxel sample of the same
+           workload (test infrastructure; never used by the GPU path).
+
+--impl reference times that oracle alone, as the reference arm, on the same
+workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FLOP_PER_PAIR = 13
+FMA_LANES_PER_SM = 128   # fp32 FMA-pipe results per SM per clock
+MUFU_LANES_PER_SM = 16   # sin/cos results per SM per clock (measured on GB300)
+FMA_PER_PAIR = 7         # k.x (1 FMUL + 2 FFMA) + complex MAC (4 FFMA)
+MUFU_PER_PAIR = 2        # sin, cos
+L2_BYTES = 129 * 1024 * 1024
+
+WORKLOAD_NAMES = {
+    1: "2D 32x32 voxels x 2048 spiral samples, F^H D",
+    2: "64^3 voxels x 16384 uniform-random samples, F^H D",
+    3: "128^3 voxels x 262144 stack-of-spirals samples, F^H D",
+    4: "256^3 voxels x 100000 kooshball samples, F^H D",
+    5: "128^3 voxels x 262144 stack-of-spirals samples, F^H F rho",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--mode", choices=["fast", "accurate"], default="fast")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- workload
+def load_workload(i: int):
+    from inputs import make_workload
+
+    return make_workload(i)
+
+
+def peak_pairs_per_s(sms: int, mhz: float) -> float:
+    per_clk = min(FMA_LANES_PER_SM / FMA_PER_PAIR, MUFU_LANES_PER_SM / MUFU_PER_PAIR)
+    return sms * per_clk * mhz * 1e6
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def oracle_sample(p, seconds: float):
+    """Time the fp64 oracle on a strided voxel sample sized for about `seconds`."""
+    import oracle
+
+    orc = oracle.get()
+    D = None if p.op == "fhf" else (p.Dr, p.Di)
+    # calibrate on a small sample
+    n_cal = max(1, min(p.N, int(2e7 // max(p.M, 1))))
+    idx = np.linspace(0, p.N - 1, n_cal).astype(np.int64)
+    t0 = time.perf_counter()
+    if D is not None:
+        orc.adjoint(p.kx, p.ky, p.kz, D, p.x[idx], p.y[idx], p.z[idx])
+    else:
+        orc.adjoint(p.kx, p.ky, p.kz, (p.rho_r[: p.M], p.rho_i[: p.M]), p.x[idx], p.y[idx], p.z[idx])
+    dt = max(time.perf_counter() - t0, 1e-6)
+    rate = n_cal * p.M / dt
+    n = int(min(p.N, max(n_cal, seconds * rate / p.M)))
+    idx = np.linspace(0, p.N - 1, n).astype(np.int64)
+    t0 = time.perf_counter()
+    if D is not None:
+        orc.adjoint(p.kx, p.ky, p.kz, D, p.x[idx], p.y[idx], p.z[idx])
+    else:
+        orc.adjoint(p.kx, p.ky, p.kz, (p.rho_r[: p.M], p.rho_i[: p.M]), p.x[idx], p.y[idx], p.z[idx])
+    dt = time.perf_counter() - t0
+    return {"value": n * p.M / dt, "unit": "pairs/s", "cores": orc.threads(), "kind": "oracle",
+            "sample": f"{n} of {p.N} voxels (evenly spaced) x all {p.M} samples, adjoint sum, fp64, "
+                      f"{dt:.1f} s", "seconds": dt, "pairs": n * p.M}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the fp64 CPU oracle, bounded sample per step, rank 0 only."""
+    if rank != 0:
+        return
+    p = load_workload(args.workload)
+    per_step = max(1.0, 60.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        oracle_sample(p, min(per_step, 2.0))
+    vals, secs, last = [], [], None
+    for _ in range(args.steps):
+        last = oracle_sample(p, per_step)
+        vals.append(last["pairs"])
+        secs.append(last["seconds"])
+    value = sum(vals) / sum(secs)
+    line = {
+        "impl": "reference", "metric": "F^H D voxel-sample pairs/s", "value": value, "unit": "pairs/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(secs) / len(secs), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "gflops": FLOP_PER_PAIR * value / 1e9,
+        "config": {"workload": WORKLOAD_NAMES[args.workload], "N": p.N, "M": p.M},
+        "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": f"per step: {last['sample']}"},
+        "e2e": {"value": value, "unit": "pairs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args, world, rank, local):
+    import torch
+
+    import non_cartesian_mri_gather_gb300 as fhd
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fhd.load()
+    mode = fhd.MODE_FAST if args.mode == "fast" else fhd.MODE_ACCURATE
+    p = load_workload(args.workload)
+    if p.op == "fhf":
+        raise SystemExit("bench.py times the F^H D workloads 1-4; workload 5 is covered by the tests")
+    names = ("kx", "ky", "kz", "Dr", "Di", "x", "y", "z")
+    host = {k: torch.from_numpy(getattr(p, k)) for k in names}
+    d = {k: v.to(dev) for k, v in host.items()}
+    rho_r = torch.empty(p.N, dtype=torch.float32, device=dev)
+    rho_i = torch.empty(p.N, dtype=torch.float32, device=dev)
+    ws = fhd.Workspace(fhd.OP_FHD, p.N, p.M, local)
+    stream = torch.cuda.current_stream(dev)
+    shape = fhd.fhd_launch_shape(local, mode)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    input_bytes = sum(v.numel() * 4 for v in d.values())
+
+    def step(e0=None, e1=None):
+        if e0 is None:
+            fhd.fhd_compute(d["kx"], d["ky"], d["kz"], d["Dr"], d["Di"], d["x"], d["y"], d["z"], rho_r, rho_i,
+                            mode=mode, workspace=ws)
+        else:
+            fhd.fhd_compute_profiled(d["kx"], d["ky"], d["kz"], d["Dr"], d["Di"], d["x"], d["y"], d["z"], rho_r,
+                                     rho_i, mode, ws, e0, e1)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fhd.fhd_workspace_status(ws) != 0:
+        raise SystemExit("kernel reported a pipeline timeout during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in ev:  # create the CUDA events before the timed region
+        e0.record(stream)
+        e1.record(stream)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    start.record(stream)
+    for e0, e1 in ev:
+        step(e0, e1)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    status = fhd.fhd_workspace_status(ws)
+    if status != 0:
+        raise SystemExit(f"kernel status {status} in the timed region")
+    ms_local = start.elapsed_time(stop) / args.steps
+    ms = max_over_ranks(ms_local, world)
+    gather_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    pairs = p.N * p.M
+    value = world * pairs / (ms * 1e-3)
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: v.pin_memory() for k, v in host.items()}
+        out_r = torch.empty(p.N, dtype=torch.float32).pin_memory()
+        out_i = torch.empty(p.N, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            for k in names:
+                d[k].copy_(pin[k], non_blocking=True)
+            step()
+            out_r.copy_(rho_r, non_blocking=True)
+            out_i.copy_(rho_i, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        k2 = max(1, min(args.steps, 3))
+        barrier(world)
+        torch.cuda.synchronize()
+        s2, t2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(k2):
+            e2e_step()
+        t2.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = max_over_ranks(s2.elapsed_time(t2) / k2, world)
+        e2e = {"value": world * pairs / (ms_e2e * 1e-3), "unit": "pairs/s", "h2d_bytes_per_step": input_bytes,
+               "d2h_bytes_per_step": 2 * p.N * 4, "ms_per_step": ms_e2e, "steps": k2}
+
+    if rank != 0:
+        return
+
+    # ---- roofline of the gather kernel (plain-ALU bound)
+    peaks = measured_peaks()
+    max_mhz = float(peaks.get("sm_max_mhz") or clk.get("sm_max_mhz") or 2070.0)
+    peak = peak_pairs_per_s(sms, max_mhz)
+    achieved = pairs / (gather_ms * 1e-3)
+    roof = {
+        "bound": "alu",
+        "achieved": FLOP_PER_PAIR * achieved / 1e12,
+        "peak": FLOP_PER_PAIR * peak / 1e12,
+        "unit": "TFLOP/s",
+        "frac": achieved / peak,
+        "traffic": None,
+        "kernel": "gather_kernel",
+        "kernel_ms": gather_ms,
+        "peak_basis": (f"{sms} SMs x {max_mhz:.0f} MHz x min({FMA_LANES_PER_SM}/{FMA_PER_PAIR}, "
+                       f"{MUFU_LANES_PER_SM}/{MUFU_PER_PAIR}) pairs/clk x {FLOP_PER_PAIR} flop/pair"),
+    }
+    if clk.get("sm_mhz"):
+        roof["frac_at_sampled_clock"] = achieved / peak_pairs_per_s(sms, clk["sm_mhz"])
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = oracle_sample(p, args.cpu_seconds)
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    line = {
+        "metric": "F^H D voxel-sample pairs/s",
+        "value": value,
+        "unit": "pairs/s",
+        "gflops": FLOP_PER_PAIR * value / 1e9,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "mode": args.mode,
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD_NAMES[args.workload],
+            "N": p.N,
+            "M": p.M,
+            "pairs_per_step": pairs,
+            "flop_per_pair": FLOP_PER_PAIR,
+            "l2": f"inputs exceed L2 ({input_bytes / 2**20:.0f} MiB of inputs vs {L2_BYTES / 2**20:.0f} MiB L2)"
+                  if input_bytes > L2_BYTES else "inputs fit in L2 (no flush)",
+            "launch": shape,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_init()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

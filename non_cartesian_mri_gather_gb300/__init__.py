@@ -187,16 +187,26 @@ def fhd_compute(kx, ky, kz, Dr, Di, x, y, z, rho_r=None, rho_i=None, mode=MODE_A
     return rho_r, rho_i
 
 
+def _event_handle(ev, stream):
+    """cudaEvent_t of a torch.cuda.Event; torch creates the CUDA event lazily on
+    its first record(), so an unused event is recorded once to create it."""
+    import torch
+
+    if ev.cuda_event == 0:
+        ev.record(stream if stream is not None else torch.cuda.current_stream())
+    return ev.cuda_event
+
+
 def fhd_compute_profiled(kx, ky, kz, Dr, Di, x, y, z, rho_r, rho_i, mode, workspace, gather_start, gather_stop,
                          stream=None):
     """fhd_compute recording two torch.cuda.Event objects around the gather kernel."""
     lib = load()
     _require((kx, ky, kz, Dr, Di, x, y, z, rho_r, rho_i), "fhd_compute_profiled")
     N, M = _n(x), _n(kx)
+    e0, e1 = _event_handle(gather_start, stream), _event_handle(gather_stop, stream)
     _check(lib.fhd_compute_profiled(M, _ptr(kx), _ptr(ky), _ptr(kz), _ptr(Dr), _ptr(Di), N, _ptr(x), _ptr(y),
                                     _ptr(z), _ptr(rho_r), _ptr(rho_i), mode, workspace.ptr, workspace.nbytes,
-                                    _stream_ptr(stream), gather_start.cuda_event, gather_stop.cuda_event),
-           "fhd_compute_profiled")
+                                    _stream_ptr(stream), e0, e1), "fhd_compute_profiled")
     return rho_r, rho_i
 
 

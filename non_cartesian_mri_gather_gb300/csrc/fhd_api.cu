@@ -40,9 +40,9 @@ cudaError_t max_ctas(int device, fhd_mode mode, int* out) {
     int per_sm = 0;
     const size_t smem = sizeof(GatherSmem);
     if (mode == FHD_MODE_FAST)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<kFast>, kCtaThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<kFast, kFastPolySlots>, kCtaThreads, smem);
     else
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<kAccurate>, kCtaThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<kAccurate, 0>, kCtaThreads, smem);
     if (e != cudaSuccess) return e;
     per_sm = std::min(std::max(per_sm, 1), kMinCtasPerSm);
     *out = sms * per_sm;
@@ -157,7 +157,8 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     const int pack_grid = (int)std::min<int64_t>(ceil_div(padded, 256), (int64_t)sms * 8);
-    pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, g.sign, g.n_sources, padded,
+    const float scale = g.sign * (mode == FHD_MODE_FAST ? 6.28318530717958647692f : 1.0f);
+    pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, scale, g.n_sources, padded,
                                                 packed, status, first_pass ? 1 : 0);
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
 
@@ -177,11 +178,11 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     if (ev_start && (e = cudaEventRecord(ev_start, stream)) != cudaSuccess) return FHD_ERR_CUDA;
     const size_t smem = sizeof(GatherSmem);
     if (mode == FHD_MODE_FAST) {
-        cudaFuncSetAttribute(gather_kernel<kFast>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        gather_kernel<kFast><<<sch.ctas, kCtaThreads, smem, stream>>>(a);
+        cudaFuncSetAttribute(gather_kernel<kFast, kFastPolySlots>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        gather_kernel<kFast, kFastPolySlots><<<sch.ctas, kCtaThreads, smem, stream>>>(a);
     } else {
-        cudaFuncSetAttribute(gather_kernel<kAccurate>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        gather_kernel<kAccurate><<<sch.ctas, kCtaThreads, smem, stream>>>(a);
+        cudaFuncSetAttribute(gather_kernel<kAccurate, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        gather_kernel<kAccurate, 0><<<sch.ctas, kCtaThreads, smem, stream>>>(a);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
     if (sch.ctas > 1) {

@@ -40,19 +40,45 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "sincos_poly.cuh"
+
 namespace fhd {
 
 // ---------------------------------------------------------------- shape
-constexpr int kThreads = 256;            // consumer threads per CTA
+// Compile-time launch shape (overridable with -D for tuning builds).
+#ifndef FHD_THREADS
+#define FHD_THREADS 512
+#endif
+#ifndef FHD_V
+#define FHD_V 8
+#endif
+#ifndef FHD_TILE
+#define FHD_TILE 128
+#endif
+#ifndef FHD_STAGES
+#define FHD_STAGES 4
+#endif
+#ifndef FHD_MIN_CTAS_PER_SM
+#define FHD_MIN_CTAS_PER_SM 1
+#endif
+#ifndef FHD_FAST_POLY_SLOTS
+#define FHD_FAST_POLY_SLOTS 1
+#endif
+#ifndef FHD_UNROLL
+#define FHD_UNROLL 2
+#endif
+constexpr int kThreads = FHD_THREADS;    // consumer threads per CTA
 constexpr int kWarps = kThreads / 32;    // consumer warps
-constexpr int kV = 8;                    // targets per consumer thread
+constexpr int kV = FHD_V;                // targets per consumer thread
 constexpr int kTargetsPerBlock = kThreads * kV;
-constexpr int kTile = 128;               // sources per staged tile
-constexpr int kStages = 4;               // shared-memory ring depth
+constexpr int kTile = FHD_TILE;          // sources per staged tile
+constexpr int kStages = FHD_STAGES;      // shared-memory ring depth
 constexpr int kRecordBytes = 32;         // one packed source
 constexpr int kTileBytes = kTile * kRecordBytes;
 constexpr int kCtaThreads = kThreads + 32;  // + one producer warp
-constexpr int kMinCtasPerSm = 2;
+constexpr int kMinCtasPerSm = FHD_MIN_CTAS_PER_SM;
+constexpr int kUnroll = FHD_UNROLL;      // sources per unrolled inner-loop step
+static_assert(kThreads % 32 == 0 && kTile % 2 == 0 && kStages >= 2, "bad launch shape");
 
 // status word bits
 constexpr uint32_t kStatusConsumerTimeout = 1u;
@@ -60,6 +86,8 @@ constexpr uint32_t kStatusProducerTimeout = 2u;
 constexpr uint32_t kStatusDrainTimeout = 4u;
 
 enum Mode : int { kAccurate = 0, kFast = 1 };
+constexpr int kFastPolySlots = FHD_FAST_POLY_SLOTS;  // of kV: share of sin/cos moved to the FMA pipe
+static_assert(kFastPolySlots >= 0 && kFastPolySlots <= kV, "bad polynomial split");
 
 // Static schedule shared by the gather and fix-up kernels (and by the
 // host-side schedule check).  The work items (target block b, source tile j)
@@ -177,31 +205,60 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 }
 
 // ---------------------------------------------------------------- per-pair math
-// exp(+i 2 pi p) for the fp32 phase p (cycles): p is reduced by its nearest
-// integer (t = p - rint(p), exact in fp32 for |p| < 2^23), then
-//   accurate: sincospif(2 t)             (sin, cos of 2 pi t)
-//   fast:     __sinf/__cosf(2 pi t)      (hardware approximations)
-template <int MODE>
-__device__ __forceinline__ void unit_phasor(float p, float& s, float& c) {
-    const float t = p - rintf(p);
-    if constexpr (MODE == kAccurate) {
-        sincospif(2.0f * t, &s, &c);
-    } else {
-        const float a = 6.28318530717958647692f * t;
-        s = __sinf(a);
-        c = __cosf(a);
-    }
+// Rounding to the nearest integer with the FMA pipe: for |v| < 2^22,
+// (v + 1.5*2^23) - 1.5*2^23 == rint(v) in round-to-nearest-even (the sum's ulp
+// is 1).  rintf() itself issues on the same 16-lane/SM/clock pipe as the
+// hardware sin/cos approximations on this GPU, so it is avoided.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+
+// Accurate mode (phase p in cycles): t = p - rint(p) is exact in fp32 for
+// |p| < 2^22, and sincospif(2t) gives sin, cos of 2 pi t.
+__device__ __forceinline__ void phasor_accurate(float p, float& s, float& c) {
+    const float r = (p + kRoundMagic) - kRoundMagic;
+    const float t = p - r;
+    sincospif(2.0f * t, &s, &c);
+}
+
+// Fast mode, MUFU pipe (phase P in radians: 2 pi is folded into the packed
+// source coordinates): hardware sin/cos approximations.  The argument is not
+// reduced; the fp32 rounding of P (|P| up to a few hundred radians for the
+// supported k ranges) stays far below the fast-mode tolerance.
+__device__ __forceinline__ void phasor_mufu(float P, float& s, float& c) {
+    s = __sinf(P);
+    c = __cosf(P);
+}
+
+// Fast mode, FMA pipe (phase P in radians): theta = P - 2 pi rint(P / 2 pi) in
+// [-pi, pi] (one-constant reduction; its error is r * |2pi - fl(2pi)| <=
+// 2e-5 rad for |P| <= 700), then the half-angle polynomial of
+// sincos_poly.cuh: sin = S*C, cos = 1 - S*S.
+__device__ __forceinline__ void phasor_poly(float P, float& s, float& c) {
+    const float q = fmaf(P, 0.159154943091895335769f, kRoundMagic);
+    const float r = q - kRoundMagic;
+    const float th = fmaf(r, -6.28318530717958647692f, P);
+    const float w = th * th;
+    float ps = poly::kSin[poly::kSinTerms - 1];
+#pragma unroll
+    for (int i = poly::kSinTerms - 2; i >= 0; --i) ps = fmaf(ps, w, poly::kSin[i]);
+    const float S = ps * th;
+    float pc = poly::kCos[poly::kCosTerms - 1];
+#pragma unroll
+    for (int i = poly::kCosTerms - 2; i >= 0; --i) pc = fmaf(pc, w, poly::kCos[i]);
+    s = S * pc;
+    c = fmaf(-S, S, 1.0f);
 }
 
 // ---------------------------------------------------------------- pack
-// Source records {sign*a.x, sign*a.y, sign*a.z, w.re, w.im, 0, 0, 0}.
+// Source records {scale*a.x, scale*a.y, scale*a.z, w.re, w.im, 0, 0, 0};
+// scale is +-1 (accurate mode, phase in cycles) or +-2 pi (fast mode, phase
+// in radians), negative for the forward sum.
 // Records n..n_padded-1 are zero (weight 0, so they add exactly 0).
 // With `reset_status`, block 0 thread 0 also clears the status word (stream
 // order puts this before the gather kernel); the second pass of F^H F rho
 // keeps the word so a timeout of the first pass stays visible.
 __global__ void pack_sources(const float* __restrict__ ax, const float* __restrict__ ay,
                              const float* __restrict__ az, const float* __restrict__ wr,
-                             const float* __restrict__ wi, float sign, int64_t n, int64_t n_padded,
+                             const float* __restrict__ wi, float scale, int64_t n, int64_t n_padded,
                              float4* __restrict__ out, uint32_t* status, int reset_status) {
     if (reset_status && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_padded;
@@ -209,7 +266,7 @@ __global__ void pack_sources(const float* __restrict__ ax, const float* __restri
         float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f);
         float4 r1 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < n) {
-            r0 = make_float4(sign * ax[i], sign * ay[i], sign * az[i], wr[i]);
+            r0 = make_float4(scale * ax[i], scale * ay[i], scale * az[i], wr[i]);
             r1.x = wi[i];
         }
         out[2 * i] = r0;
@@ -220,11 +277,19 @@ __global__ void pack_sources(const float* __restrict__ ax, const float* __restri
 // ---------------------------------------------------------------- gather
 struct __align__(16) GatherSmem {
     float4 ring[kStages][kTile * 2];
+    // Running sums of the current segment, one private column per consumer
+    // thread (rows: kV real parts, then kV imaginary parts).  They are touched
+    // once per tile, so keeping them here instead of in registers frees
+    // 2*kV registers per thread for more resident warps.
+    float run[2 * kV][kThreads];
     uint64_t full[kStages];
     uint64_t empty[kStages];
 };
 
-template <int MODE>
+// MODE: kAccurate or kFast.  NPOLY (fast mode only): how many of the kV
+// register slots evaluate sin/cos with the FMA-pipe polynomial instead of the
+// MUFU pipe; it sets the split between the two pipes.
+template <int MODE, int NPOLY>
 __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(const GatherArgs args) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     GatherSmem& sm = *reinterpret_cast<GatherSmem*>(smem_raw);
@@ -278,7 +343,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
 
     // ---------------------------------------------------- consumer warps
     float bx[kV], by[kV], bz[kV];
-    float acc_r[kV], acc_i[kV];
+    const int tid = threadIdx.x;
     int64_t seg_first_tile = 0;  // first tile index of the current segment
     int64_t consumed = 0;
 
@@ -296,8 +361,8 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
                 bx[v] = in ? args.tx[t] : 0.f;
                 by[v] = in ? args.ty[t] : 0.f;
                 bz[v] = in ? args.tz[t] : 0.f;
-                acc_r[v] = 0.f;
-                acc_i[v] = 0.f;
+                sm.run[v][tid] = 0.f;
+                sm.run[kV + v][tid] = 0.f;
             }
         }
 
@@ -316,7 +381,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
             ti[v] = 0.f;
         }
         const float4* rec = &sm.ring[st][0];
-#pragma unroll 2
+#pragma unroll kUnroll
         for (int s = 0; s < kTile; ++s) {
             const float4 a = rec[2 * s];                                         // a.x a.y a.z w.re
             const float wim = reinterpret_cast<const float*>(rec)[8 * s + 4];   // w.im
@@ -324,7 +389,13 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
             for (int v = 0; v < kV; ++v) {
                 const float p = fmaf(a.z, bz[v], fmaf(a.y, by[v], a.x * bx[v]));
                 float sn, cs;
-                unit_phasor<MODE>(p, sn, cs);
+                if constexpr (MODE == kAccurate) {
+                    phasor_accurate(p, sn, cs);
+                } else if (v >= kV - NPOLY) {
+                    phasor_poly(p, sn, cs);
+                } else {
+                    phasor_mufu(p, sn, cs);
+                }
                 tr[v] = fmaf(a.w, cs, tr[v]);
                 tr[v] = fmaf(-wim, sn, tr[v]);
                 ti[v] = fmaf(a.w, sn, ti[v]);
@@ -333,8 +404,8 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
         }
 #pragma unroll
         for (int v = 0; v < kV; ++v) {
-            acc_r[v] += tr[v];
-            acc_i[v] += ti[v];
+            sm.run[v][tid] += tr[v];
+            sm.run[kV + v][tid] += ti[v];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[st]);
@@ -348,8 +419,8 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
                 for (int v = 0; v < kV; ++v) {
                     const int64_t t = base + (int64_t)v * kThreads;
                     if (t < sch.n_targets) {
-                        args.out_r[t] = acc_r[v];
-                        args.out_i[t] = acc_i[v];
+                        args.out_r[t] = sm.run[v][tid];
+                        args.out_i[t] = sm.run[kV + v][tid];
                     }
                 }
             } else {
@@ -358,8 +429,8 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
                 float* pi = pr + kTargetsPerBlock;
 #pragma unroll
                 for (int v = 0; v < kV; ++v) {
-                    pr[threadIdx.x + v * kThreads] = acc_r[v];
-                    pi[threadIdx.x + v * kThreads] = acc_i[v];
+                    pr[tid + v * kThreads] = sm.run[v][tid];
+                    pi[tid + v * kThreads] = sm.run[kV + v][tid];
                 }
             }
         }
