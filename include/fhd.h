@@ -30,7 +30,8 @@
  * Ownership  all pointers are owned by the caller and must be device memory
  *            of the current CUDA device (cudaMalloc'd or managed).  The
  *            library allocates no memory, keeps no pointer after a call
- *            returns and holds no global state.
+ *            returns and holds no global state (the one exception is the
+ *            static scratch array of fhd_compute_noalloc, described there).
  * Outputs    are overwritten, never accumulated into.  Outputs must not
  *            overlap any input, each other, or the workspace.
  * Async      a call validates its arguments on the host, enqueues its kernels
@@ -75,7 +76,8 @@ typedef enum {
     FHD_ERR_WORKSPACE = 4,     /* workspace smaller than fhd_workspace_bytes() */
     FHD_ERR_CUDA = 5,          /* a CUDA runtime call failed (see cudaGetLastError) */
     FHD_ERR_TIMEOUT = 6,       /* a kernel's bounded pipeline wait expired (status word) */
-    FHD_ERR_RANGE = 7          /* an array extends past the end of its device allocation */
+    FHD_ERR_RANGE = 7,         /* an array extends past the end of its device allocation */
+    FHD_ERR_TOO_LARGE = 8      /* fhd_compute_noalloc: problem exceeds its static scratch */
 } fhd_status;
 
 typedef enum {
@@ -175,6 +177,47 @@ const char *fhd_status_string(fhd_status status);
  */
 fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *threads,
                             int *targets_per_thread, int *tile_sources, int *stages);
+
+/*
+ * F^H D without any allocation, for callers that cannot allocate device
+ * memory.  The operation, argument meaning, layout, validation and results
+ * are those of fhd_compute, but there is no workspace argument: the scratch
+ * space (packed sample records, per-CTA partial sums, status word) is a
+ * file-scope static device array of FHD_NOALLOC_SCRATCH_BYTES inside the
+ * library.  The pages this library implements have no counterpart of this
+ * entry point; it exists for deployment.
+ *
+ * Who needs it: callers that must not allocate device memory after start-up,
+ * for example a scanner's real-time reconstruction loop running under a
+ * device-memory budget fixed at start-up (cudaMalloc can synchronise the
+ * device and can fail under memory pressure), or a host application that
+ * hands this library its data buffers but owns no allocator it may call.
+ *
+ * Limits: M <= FHD_NOALLOC_MAX_SAMPLES samples, and a device with at most
+ * FHD_NOALLOC_MAX_CTAS resident gather CTAs (a GB300 uses 152).  Larger
+ * problems return FHD_ERR_TOO_LARGE before anything is launched; N is not
+ * limited.
+ *
+ * Memory: every GPU that loads the library holds the array (about 16 MiB)
+ * until the process exits.  The first call on a device, with that device
+ * current, looks up the array's device address (cudaGetSymbolAddress) and
+ * caches it; make that first call before any stream capture begins.
+ *
+ * Sharing: all calls on a device use the same array, which keeps the last
+ * call's contents.  Everything a call reads from it is written earlier in
+ * the same call (the status word is cleared first), so stale contents do
+ * not leak into results, but calls whose kernels overlap on the GPU (other
+ * streams, other host threads) race on the array: serialise them, e.g. on one
+ * stream.  fhd_workspace_status() does not apply to this entry point.
+ */
+#define FHD_NOALLOC_MAX_SAMPLES 131072
+#define FHD_NOALLOC_MAX_CTAS 192
+#define FHD_NOALLOC_SCRATCH_BYTES (512 + (size_t)FHD_NOALLOC_MAX_SAMPLES * 32 + \
+                                   (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * 4096 * 4)
+fhd_status fhd_compute_noalloc(int64_t M, const float *kx, const float *ky, const float *kz,
+                               const float *Dr, const float *Di,
+                               int64_t N, const float *x, const float *y, const float *z,
+                               float *rho_r, float *rho_i, fhd_mode mode, fhd_stream_t stream);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int fhd_version(void);

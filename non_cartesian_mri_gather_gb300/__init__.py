@@ -39,6 +39,7 @@ __all__ = [
     "fhd_status_string",
     "fhd_launch_shape",
     "fhd_version",
+    "fhd_compute_noalloc",
     "Workspace",
 ]
 
@@ -55,6 +56,7 @@ STATUS_NAMES = {
     5: "FHD_ERR_CUDA",
     6: "FHD_ERR_TIMEOUT",
     7: "FHD_ERR_RANGE",
+    8: "FHD_ERR_TOO_LARGE",
 }
 
 _lib = None
@@ -76,6 +78,7 @@ SIGNATURES = {
     "fhd_status_string": (ctypes.c_char_p, [_int]),
     "fhd_launch_shape": (_int, [_int, _int, _vp, _vp, _vp, _vp, _vp]),
     "fhd_version": (_int, []),
+    "fhd_compute_noalloc": (_int, [_i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp]),
     "fhd_test_compute_skip_tile": (_int, [_i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp,
                                           _sz, _vp, _i64]),
     "fhd_test_schedule": (_int, [_i64, _i64, _int]),
@@ -245,6 +248,19 @@ def fhfrho_apply(x, y, z, rho_r, rho_i, kx, ky, kz, out_r=None, out_i=None, mode
                             _ptr(kz), _ptr(out_r), _ptr(out_i), mode, ws.ptr, ws.nbytes, _stream_ptr(stream)),
            "fhfrho_apply")
     return out_r, out_i
+
+
+def fhd_compute_noalloc(kx, ky, kz, Dr, Di, x, y, z, rho_r, rho_i, mode=MODE_ACCURATE, stream=None):
+    """rho = F^H D through the entry point that allocates nothing (its scratch is
+    a static device array in the library; see fhd_compute_noalloc in fhd.h).
+    The outputs must be given: this path allocates no tensors either."""
+    lib = load()
+    _require((kx, ky, kz, Dr, Di, x, y, z, rho_r, rho_i), "fhd_compute_noalloc")
+    N, M = _n(x), _n(kx)
+    _check(lib.fhd_compute_noalloc(M, _ptr(kx), _ptr(ky), _ptr(kz), _ptr(Dr), _ptr(Di), N, _ptr(x), _ptr(y),
+                                   _ptr(z), _ptr(rho_r), _ptr(rho_i), mode, _stream_ptr(stream)),
+           "fhd_compute_noalloc")
+    return rho_r, rho_i
 
 
 def fhd_workspace_status(workspace, stream=None) -> int:

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "../../include/fhd.h"
@@ -21,7 +22,7 @@ constexpr size_t kWsAlign = 256;
 constexpr size_t kHeaderBytes = 256;  // status word + reserved
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
 
-size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -364,6 +365,7 @@ const char* fhd_status_string(fhd_status s) {
         case FHD_ERR_CUDA: return "CUDA runtime error";
         case FHD_ERR_TIMEOUT: return "kernel pipeline wait timed out";
         case FHD_ERR_RANGE: return "array extends past the end of its device allocation";
+        case FHD_ERR_TOO_LARGE: return "problem exceeds the static scratch of fhd_compute_noalloc";
     }
     return "unknown status";
 }
@@ -385,6 +387,72 @@ fhd_status fhd_launch_shape(int device, fhd_mode mode, int* ctas, int* threads, 
 }
 
 int fhd_version(void) { return kVersion; }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation variant
+// fhd_compute for callers that cannot allocate device memory (see include/fhd.h):
+// the scratch that fhd_compute takes from the caller's workspace lives in this
+// static device array instead.  Layout inside it is the same layout_for()
+// layout fhd_compute uses, which fits because M and the resident CTA count are
+// capped; everything the kernels read from it is written earlier in the same
+// call (pack_sources clears the status word and rewrites every record; each
+// partial slot the fix-up reads is written by its CTA first).
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = FHD_NOALLOC_SCRATCH_BYTES;
+static_assert(kNoAllocScratchBytes >= kHeaderBytes + (size_t)FHD_NOALLOC_MAX_SAMPLES * kRecordBytes + kWsAlign +
+                                          (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * kTargetsPerBlock * sizeof(float),
+              "static scratch smaller than the layout it must hold");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the static scratch on `device` (the current device):
+// looked up once per device with cudaGetSymbolAddress, then cached.  In host
+// code g_noalloc_scratch names a host-side stand-in, never the device array.
+fhd_status noalloc_scratch(int device, void** out) {
+    if (device < 0 || device >= kNoAllocMaxDevices) return FHD_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[device] == nullptr) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return FHD_ERR_CUDA;
+        }
+        g_noalloc_ptr[device] = p;
+    }
+    *out = g_noalloc_ptr[device];
+    return FHD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fhd_status fhd_compute_noalloc(int64_t M, const float* kx, const float* ky, const float* kz, const float* Dr,
+                               const float* Di, int64_t N, const float* x, const float* y, const float* z,
+                               float* rho_r, float* rho_i, fhd_mode mode, fhd_stream_t stream) {
+    if (N < 0 || M < 0 || !valid_mode(mode)) return FHD_ERR_INVALID_VALUE;
+    if (M > FHD_NOALLOC_MAX_SAMPLES) return FHD_ERR_TOO_LARGE;
+    if (N == 0) return FHD_OK;
+    int device = 0, sms = 0;
+    if (cudaGetDevice(&device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        cudaGetLastError();
+        return FHD_ERR_CUDA;
+    }
+    if ((int64_t)sms * kMinCtasPerSm > FHD_NOALLOC_MAX_CTAS) return FHD_ERR_TOO_LARGE;
+    void* scratch = nullptr;
+    const fhd_status s = noalloc_scratch(device, &scratch);
+    if (s != FHD_OK) return s;
+    return fhd_compute_impl(M, kx, ky, kz, Dr, Di, N, x, y, z, rho_r, rho_i, mode, scratch, kNoAllocScratchBytes,
+                            (cudaStream_t)stream, nullptr, nullptr, -1);
+}
 
 // Declared in include/fhd_testing.h.
 fhd_status fhd_test_check_array(const void* p, size_t bytes, int device) {
