@@ -174,6 +174,37 @@ def peak_pairs_per_s(sms: int, mhz: float) -> float:
     return sms * per_clk * mhz * 1e6
 
 
+KERNEL_SOURCES = ("non_cartesian_mri_gather_gb300/csrc/fhd_kernels.cuh",
+                  "non_cartesian_mri_gather_gb300/csrc/sincos_poly.cuh",
+                  "non_cartesian_mri_gather_gb300/csrc/fhd_api.cu")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gather_kernel_fast_256cube_100k_dram.md")
+
+
+def profiled_traffic(workload: int, mode: str):
+    """DRAM bytes per gather launch from the committed ncu summary, or None when
+    the summary is for another workload/mode or the kernel sources changed since."""
+    import hashlib
+
+    if workload != 4 or mode != "fast":
+        return None
+    try:
+        fields = {}
+        with open(TRAFFIC_PROFILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith(("|", " ", "#")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        h = hashlib.sha256()
+        for rel in KERNEL_SOURCES:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != fields.get("kernel_sources_sha256"):
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -347,7 +378,8 @@ def run_ours(args, world, rank, local):
         "peak": FLOP_PER_PAIR * peak / 1e12,
         "unit": "TFLOP/s",
         "frac": achieved / peak,
-        "traffic": None,
+        "traffic": profiled_traffic(args.workload, args.mode),
+        "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
         "kernel": "gather_kernel",
         "kernel_ms": gather_ms,
         "peak_basis": (f"{sms} SMs x {max_mhz:.0f} MHz x min({FMA_LANES_PER_SM}/{FMA_PER_PAIR}, "
