@@ -14,12 +14,18 @@ value      voxel-sample pairs per second over the K timed steps, inputs resident
 e2e        the same metric through the public API with pinned HOST buffers:
            every step copies the inputs host->device, runs fhd_compute and
            copies rho back device->host, all inside the timed region.
-roofline   the gather kernel against the plain-ALU bound
-           SMs x clock x min(FMA lanes / 7, MUFU lanes / 2) pairs/s
-           (7 FMA-pipe and 2 MUFU instructions per pair), with the lane counts
-           128 and 16 per SM per clock and the maximum SM clock; the kernel's
-           duration comes from CUDA events recorded on its stream around the
-           gather and fix-up launches of every timed step.
+roofline   the gather kernel against its plain-ALU bound
+           SMs x clock x min(128 / n_fma, 16 / n_mufu, 128 / (n_fma + n_mufu))
+           pairs/s: 128 FMA-pipe lanes, 16 MUFU lanes and one warp instruction
+           issued per scheduler per clock, per SM; n_fma and n_mufu are the
+           algorithm's instructions per pair.  Pair by pair (direct): 7 and 2
+           (k.x, complex MAC; sin, cos).  Equal-spacing recurrence on the
+           benchmark's grid voxels, V = 8 targets per thread: per pair one
+           complex step (4, skipped for the first target) and two adds, plus per
+           (thread, sample) two phases (6) and D*exp(i theta_0) (4), and 4 MUFU
+           -> n_fma = 6 - 4/V + 10/V, n_mufu = 4/V.  Maximum SM clock.  The
+           kernel's duration comes from CUDA events recorded on its stream
+           around the gather and fix-up launches of every timed step.
 cpu_baseline  the fp64 CPU oracle on a bounded voxel sample of the same
            workload (test infrastructure; never used by the GPU path).
 
@@ -46,8 +52,16 @@ if ROOT not in sys.path:
 FLOP_PER_PAIR = 13
 FMA_LANES_PER_SM = 128   # fp32 FMA-pipe results per SM per clock
 MUFU_LANES_PER_SM = 16   # sin/cos results per SM per clock (measured on GB300)
-FMA_PER_PAIR = 7         # k.x (1 FMUL + 2 FFMA) + complex MAC (4 FFMA)
-MUFU_PER_PAIR = 2        # sin, cos
+ISSUE_PER_SM = 128       # 4 schedulers x 1 warp instruction (32 lanes) per clock
+TARGETS_PER_THREAD = 8
+
+
+def per_pair_counts(path: str):
+    """(FMA-pipe, MUFU) instructions per pair of the algorithm on `path`."""
+    if path == "direct":
+        return 7.0, 2.0          # k.x (1 FMUL + 2 FFMA) + complex MAC (4 FFMA); sin, cos
+    V = TARGETS_PER_THREAD
+    return 6.0 - 4.0 / V + 10.0 / V, 4.0 / V
 L2_BYTES = 129 * 1024 * 1024
 
 WORKLOAD_NAMES = {
@@ -66,7 +80,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=4, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--mode", choices=["fast", "accurate"], default="fast")
+    ap.add_argument("--mode", choices=["fast", "accurate", "fast-direct", "accurate-direct"], default="fast")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
@@ -169,8 +183,9 @@ def load_workload(i: int):
     return make_workload(i)
 
 
-def peak_pairs_per_s(sms: int, mhz: float) -> float:
-    per_clk = min(FMA_LANES_PER_SM / FMA_PER_PAIR, MUFU_LANES_PER_SM / MUFU_PER_PAIR)
+def peak_pairs_per_s(sms: int, mhz: float, path: str = "direct") -> float:
+    n_fma, n_mufu = per_pair_counts(path)
+    per_clk = min(FMA_LANES_PER_SM / n_fma, MUFU_LANES_PER_SM / n_mufu, ISSUE_PER_SM / (n_fma + n_mufu))
     return sms * per_clk * mhz * 1e6
 
 
@@ -186,7 +201,7 @@ def profiled_traffic(workload: int, mode: str):
     import hashlib
 
     if workload != 4 or mode != "fast":
-        return None
+        return None  # the committed capture is of the default workload and mode
     try:
         fields = {}
         with open(TRAFFIC_PROFILE) as f:
@@ -281,7 +296,11 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     fhd.load()
-    mode = fhd.MODE_FAST if args.mode == "fast" else fhd.MODE_ACCURATE
+    mode = {"fast": fhd.MODE_FAST, "accurate": fhd.MODE_ACCURATE, "fast-direct": fhd.MODE_FAST_DIRECT,
+            "accurate-direct": fhd.MODE_ACCURATE_DIRECT}[args.mode]
+    # The benchmark voxels are power-of-two grids: every thread's 8 consecutive
+    # voxels are exactly equally spaced, so the recurrence runs unless disabled.
+    path = "direct" if args.mode.endswith("direct") else "recurrence"
     p = load_workload(args.workload)
     if p.op == "fhf":
         raise SystemExit("bench.py times the F^H D workloads 1-4; workload 5 is covered by the tests")
@@ -370,8 +389,9 @@ def run_ours(args, world, rank, local):
     # ---- roofline of the gather kernel (plain-ALU bound)
     peaks = measured_peaks()
     max_mhz = float(peaks.get("sm_max_mhz") or clk.get("sm_max_mhz") or 2070.0)
-    peak = peak_pairs_per_s(sms, max_mhz)
+    peak = peak_pairs_per_s(sms, max_mhz, path)
     achieved = pairs / (gather_ms * 1e-3)
+    n_fma, n_mufu = per_pair_counts(path)
     roof = {
         "bound": "alu",
         "achieved": FLOP_PER_PAIR * achieved / 1e12,
@@ -382,11 +402,14 @@ def run_ours(args, world, rank, local):
         "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
         "kernel": "gather_kernel",
         "kernel_ms": gather_ms,
-        "peak_basis": (f"{sms} SMs x {max_mhz:.0f} MHz x min({FMA_LANES_PER_SM}/{FMA_PER_PAIR}, "
-                       f"{MUFU_LANES_PER_SM}/{MUFU_PER_PAIR}) pairs/clk x {FLOP_PER_PAIR} flop/pair"),
+        "path": path,
+        "peak_basis": (f"{sms} SMs x {max_mhz:.0f} MHz x min({FMA_LANES_PER_SM}/{n_fma:g}, "
+                       f"{MUFU_LANES_PER_SM}/{n_mufu:g}, {ISSUE_PER_SM}/{n_fma + n_mufu:g}) pairs/clk x "
+                       f"{FLOP_PER_PAIR} flop/pair ({path} path)"),
+        "direct_path_peak": FLOP_PER_PAIR * peak_pairs_per_s(sms, max_mhz, "direct") / 1e12,
     }
     if clk.get("sm_mhz"):
-        roof["frac_at_sampled_clock"] = achieved / peak_pairs_per_s(sms, clk["sm_mhz"])
+        roof["frac_at_sampled_clock"] = achieved / peak_pairs_per_s(sms, clk["sm_mhz"], path)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:

@@ -48,9 +48,17 @@
  * Modes      FHD_MODE_ACCURATE evaluates sin/cos with sincospif on the
  *            period-reduced phase (relative L2 error vs an fp64 evaluation
  *            below 1e-5 on the benchmark workloads).  FHD_MODE_FAST uses the
- *            hardware sin/cos approximations on the period-reduced phase,
- *            partly replaced by an FMA-pipe polynomial (relative L2 error
- *            below 1e-3).
+ *            hardware sin/cos approximations, partly replaced by an FMA-pipe
+ *            polynomial (relative L2 error below 1e-3).  Either may be OR-ed
+ *            with FHD_MODE_DIRECT, see below.
+ * Spacing    where a thread's 8 consecutive targets (voxels for F^H D,
+ *            samples for F rho) are exactly equally spaced, as the voxels of a
+ *            regular image grid are, the kernel evaluates two phasors per
+ *            (thread, source) and reaches the other targets by the recurrence
+ *            exp(i 2 pi k.(x0 + v d)) = exp(i 2 pi k.x0) exp(i 2 pi k.d)^v,
+ *            an exact identity evaluated in fp32 (same tolerances).  Other
+ *            targets are evaluated pair by pair.  FHD_MODE_DIRECT forces the
+ *            pair-by-pair evaluation everywhere.
  * Results are bit-identical from run to run on the same device: the sample
  * dimension is split among CTAs in a fixed way and the partial sums are
  * added in a fixed order, without atomics.
@@ -82,7 +90,10 @@ typedef enum {
 
 typedef enum {
     FHD_MODE_ACCURATE = 0,
-    FHD_MODE_FAST = 1
+    FHD_MODE_FAST = 1,
+    FHD_MODE_DIRECT = 2,          /* flag: no equal-spacing recurrence */
+    FHD_MODE_ACCURATE_DIRECT = 2,
+    FHD_MODE_FAST_DIRECT = 3
 } fhd_mode;
 
 typedef enum {

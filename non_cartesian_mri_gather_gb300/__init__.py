@@ -26,6 +26,9 @@ __all__ = [
     "FhdError",
     "MODE_ACCURATE",
     "MODE_FAST",
+    "MODE_DIRECT",
+    "MODE_ACCURATE_DIRECT",
+    "MODE_FAST_DIRECT",
     "OP_FHD",
     "OP_FWD",
     "OP_FHF",
@@ -45,6 +48,9 @@ __all__ = [
 
 MODE_ACCURATE = 0
 MODE_FAST = 1
+MODE_DIRECT = 2  # flag: evaluate every pair directly (no equal-spacing recurrence)
+MODE_ACCURATE_DIRECT = 2
+MODE_FAST_DIRECT = 3
 OP_FHD, OP_FWD, OP_FHF = 0, 1, 2
 
 STATUS_NAMES = {

@@ -26,6 +26,11 @@ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Mode word: bit 0 selects fast sin/cos, bit 1 (FHD_MODE_DIRECT) disables the
+// equal-spacing recurrence.
+bool valid_mode(fhd_mode m) { return ((int)m & ~3) == 0; }
+bool fast_mode(fhd_mode m) { return ((int)m & FHD_MODE_FAST) != 0; }
+
 struct Layout {
     size_t packed;   // offset of packed source records
     size_t partial;  // offset of per-CTA partial slots
@@ -40,7 +45,7 @@ cudaError_t max_ctas(int device, fhd_mode mode, int* out) {
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     const size_t smem = sizeof(GatherSmem);
-    if (mode == FHD_MODE_FAST)
+    if (fast_mode(mode))
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<kFast, kFastPolySlots>, kCtaThreads, smem);
     else
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<kAccurate, 0>, kCtaThreads, smem);
@@ -158,7 +163,7 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     const int pack_grid = (int)std::min<int64_t>(ceil_div(padded, 256), (int64_t)sms * 8);
-    const float scale = g.sign * (mode == FHD_MODE_FAST ? 6.28318530717958647692f : 1.0f);
+    const float scale = g.sign * (fast_mode(mode) ? 6.28318530717958647692f : 1.0f);
     pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, scale, g.n_sources, padded,
                                                 packed, status, first_pass ? 1 : 0);
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
@@ -175,10 +180,11 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     a.status = status;
     a.wait_limit_ns = kWaitLimitNs;
     a.skip_tile = skip_tile;
+    a.allow_strided = ((int)mode & FHD_MODE_DIRECT) ? 0 : 1;
 
     if (ev_start && (e = cudaEventRecord(ev_start, stream)) != cudaSuccess) return FHD_ERR_CUDA;
     const size_t smem = sizeof(GatherSmem);
-    if (mode == FHD_MODE_FAST) {
+    if (fast_mode(mode)) {
         cudaFuncSetAttribute(gather_kernel<kFast, kFastPolySlots>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         gather_kernel<kFast, kFastPolySlots><<<sch.ctas, kCtaThreads, smem, stream>>>(a);
     } else {
@@ -194,7 +200,7 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     return FHD_OK;
 }
 
-bool valid_mode(fhd_mode m) { return m == FHD_MODE_ACCURATE || m == FHD_MODE_FAST; }
+
 
 // Shared validation for the three operators.  `ins`/`outs` list every array.
 fhd_status validate(fhd_op op, int64_t N, int64_t M, fhd_mode mode, const Buf* ins, int n_in, const Buf* outs,
@@ -400,10 +406,12 @@ int fhd_version(void) { return kVersion; }
 // partial slot the fix-up reads is written by its CTA first).
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = FHD_NOALLOC_SCRATCH_BYTES;
-static_assert(kNoAllocScratchBytes >= kHeaderBytes + (size_t)FHD_NOALLOC_MAX_SAMPLES * kRecordBytes + kWsAlign +
-                                          (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * kTargetsPerBlock * sizeof(float),
-              "static scratch smaller than the layout it must hold");
+// FHD_NOALLOC_SCRATCH_BYTES is the size for the default launch shape; builds
+// with other shape constants size the array for their own layout.
+constexpr size_t kNoAllocLayoutBytes = kHeaderBytes + (size_t)FHD_NOALLOC_MAX_SAMPLES * kRecordBytes + kWsAlign +
+                                       (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * kTargetsPerBlock * sizeof(float);
+constexpr size_t kNoAllocScratchBytes =
+    FHD_NOALLOC_SCRATCH_BYTES > kNoAllocLayoutBytes ? FHD_NOALLOC_SCRATCH_BYTES : kNoAllocLayoutBytes;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

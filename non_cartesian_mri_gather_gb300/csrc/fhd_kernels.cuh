@@ -67,6 +67,7 @@ namespace fhd {
 #ifndef FHD_UNROLL
 #define FHD_UNROLL 2
 #endif
+
 constexpr int kThreads = FHD_THREADS;    // consumer threads per CTA
 constexpr int kWarps = kThreads / 32;    // consumer warps
 constexpr int kV = FHD_V;                // targets per consumer thread
@@ -88,6 +89,7 @@ constexpr uint32_t kStatusDrainTimeout = 4u;
 enum Mode : int { kAccurate = 0, kFast = 1 };
 constexpr int kFastPolySlots = FHD_FAST_POLY_SLOTS;  // of kV: share of sin/cos moved to the FMA pipe
 static_assert(kFastPolySlots >= 0 && kFastPolySlots <= kV, "bad polynomial split");
+
 
 // Static schedule shared by the gather and fix-up kernels (and by the
 // host-side schedule check).  The work items (target block b, source tile j)
@@ -137,6 +139,7 @@ struct GatherArgs {
     uint32_t* status;
     uint64_t wait_limit_ns;          // bounded-wait time limit
     int64_t skip_tile;               // test hook: work item whose copy is never issued (-1: none)
+    int allow_strided;               // 1: use the equal-spacing recurrence where it applies
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -286,6 +289,104 @@ struct __align__(16) GatherSmem {
     uint64_t empty[kStages];
 };
 
+// Sum of one staged tile into fresh per-tile accumulators tr, ti: every
+// record is read by all lanes at once (broadcast) and combined with the
+// thread's kV targets.  In fast mode the last NPOLY register slots take the
+// FMA-pipe polynomial, the others the MUFU pipe.
+template <int MODE, int NPOLY>
+__device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, const float (&bx)[kV],
+                                                const float (&by)[kV], const float (&bz)[kV], float (&tr)[kV],
+                                                float (&ti)[kV]) {
+#pragma unroll
+    for (int v = 0; v < kV; ++v) {
+        tr[v] = 0.f;
+        ti[v] = 0.f;
+    }
+#pragma unroll kUnroll
+    for (int s = 0; s < kTile; ++s) {
+        const float4 a = rec[2 * s];                                         // a.x a.y a.z w.re
+        const float wim = reinterpret_cast<const float*>(rec)[8 * s + 4];   // w.im
+#pragma unroll
+        for (int v = 0; v < kV; ++v) {
+            const float p = fmaf(a.z, bz[v], fmaf(a.y, by[v], a.x * bx[v]));
+            float sn, cs;
+            if constexpr (MODE == kAccurate) {
+                phasor_accurate(p, sn, cs);
+            } else if (v >= kV - NPOLY) {
+                phasor_poly(p, sn, cs);
+            } else {
+                phasor_mufu(p, sn, cs);
+            }
+            tr[v] = fmaf(a.w, cs, tr[v]);
+            tr[v] = fmaf(-wim, sn, tr[v]);
+            ti[v] = fmaf(a.w, sn, ti[v]);
+            ti[v] = fmaf(wim, cs, ti[v]);
+        }
+    }
+}
+
+// Equal-spacing recurrence.  When a thread's kV consecutive targets satisfy
+// b_v = b_0 + v*d exactly, exp(i 2 pi a.b_v) = exp(i 2 pi a.b_0) * w^v with
+// w = exp(i 2 pi a.d).  Per source the thread evaluates two phasors (b_0 and
+// d) and f = w_s * exp(i 2 pi a.b_0); every further target then costs one
+// complex multiply f *= w (4 FMA-pipe instructions) and two adds into its
+// accumulators, instead of a phase and a sin/cos per pair.  Voxels of a
+// regular image grid, and samples along a radial spoke, are equally spaced.
+template <int MODE>
+__device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict__ rec, float x0, float y0,
+                                                        float z0, float dx, float dy, float dz, float (&tr)[kV],
+                                                        float (&ti)[kV]) {
+#pragma unroll
+    for (int v = 0; v < kV; ++v) {
+        tr[v] = 0.f;
+        ti[v] = 0.f;
+    }
+#pragma unroll kUnroll
+    for (int s = 0; s < kTile; ++s) {
+        const float4 a = rec[2 * s];                                         // a.x a.y a.z w.re
+        const float wim = reinterpret_cast<const float*>(rec)[8 * s + 4];   // w.im
+        const float p0 = fmaf(a.z, z0, fmaf(a.y, y0, a.x * x0));
+        const float pd = fmaf(a.z, dz, fmaf(a.y, dy, a.x * dx));
+        float s0, c0, sw, cw;
+        if constexpr (MODE == kAccurate) {
+            phasor_accurate(p0, s0, c0);
+            phasor_accurate(pd, sw, cw);
+        } else {
+            phasor_mufu(p0, s0, c0);
+            phasor_mufu(pd, sw, cw);
+        }
+        float fr = fmaf(a.w, c0, -wim * s0);  // f = w_s * exp(i 2 pi a.b_0)
+        float fi = fmaf(a.w, s0, wim * c0);
+#pragma unroll
+        for (int v = 0; v < kV; ++v) {
+            tr[v] += fr;
+            ti[v] += fi;
+            if (v + 1 < kV) {
+                const float nr = fmaf(fr, cw, -fi * sw);  // f *= exp(i 2 pi a.d)
+                fi = fmaf(fr, sw, fi * cw);
+                fr = nr;
+            }
+        }
+    }
+}
+
+// True when c[v] == c[0] + v*d exactly for the first n entries, with d the
+// float32 value c[1] - c[0] (checked in double, where these sums are exact).
+__device__ __forceinline__ bool equally_spaced(const float (&c)[kV], int n, float& d) {
+    if (n < 2) {
+        d = 0.f;
+        return true;
+    }
+    const double c0 = c[0];
+    const double dd = (double)c[1] - c0;
+    d = (float)dd;
+    bool ok = (double)d == dd;
+#pragma unroll
+    for (int v = 2; v < kV; ++v)
+        if (v < n) ok = ok && ((double)c[v] == c0 + (double)v * dd);
+    return ok;
+}
+
 // MODE: kAccurate or kFast.  NPOLY (fast mode only): how many of the kV
 // register slots evaluate sin/cos with the FMA-pipe polynomial instead of the
 // MUFU pipe; it sets the split between the two pipes.
@@ -342,7 +443,10 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
     }
 
     // ---------------------------------------------------- consumer warps
+    // Thread tid owns the kV consecutive targets b*kTargetsPerBlock + tid*kV + v.
     float bx[kV], by[kV], bz[kV];
+    float sx = 0.f, sy = 0.f, sz = 0.f;  // target spacing of the strided path
+    bool strided = false;                // warp-uniform
     const int tid = threadIdx.x;
     int64_t seg_first_tile = 0;  // first tile index of the current segment
     int64_t consumed = 0;
@@ -353,10 +457,10 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
         if (w == w_begin || j == 0) {
             // new segment: this CTA's range enters target block b
             seg_first_tile = j;
-            const int64_t base = b * kTargetsPerBlock + threadIdx.x;
+            const int64_t base = b * kTargetsPerBlock + (int64_t)tid * kV;
 #pragma unroll
             for (int v = 0; v < kV; ++v) {
-                const int64_t t = base + (int64_t)v * kThreads;
+                const int64_t t = base + v;
                 const bool in = t < sch.n_targets;
                 bx[v] = in ? args.tx[t] : 0.f;
                 by[v] = in ? args.ty[t] : 0.f;
@@ -364,6 +468,11 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
                 sm.run[v][tid] = 0.f;
                 sm.run[kV + v][tid] = 0.f;
             }
+            const int n_in = (int)(sch.n_targets - base < kV ? (sch.n_targets - base > 0 ? sch.n_targets - base : 0)
+                                                             : kV);
+            const bool spaced = equally_spaced(bx, n_in, sx) && equally_spaced(by, n_in, sy) &&
+                                equally_spaced(bz, n_in, sz);
+            strided = args.allow_strided && __all_sync(0xffffffffu, spaced);
         }
 
         const int st = (int)(consumed % kStages);
@@ -375,33 +484,11 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
         // running sum once per tile, keeps fp32 rounding growth at
         // O(sqrt(kTile) + sqrt(M / kTile)) instead of O(sqrt(M)).
         float tr[kV], ti[kV];
-#pragma unroll
-        for (int v = 0; v < kV; ++v) {
-            tr[v] = 0.f;
-            ti[v] = 0.f;
-        }
         const float4* rec = &sm.ring[st][0];
-#pragma unroll kUnroll
-        for (int s = 0; s < kTile; ++s) {
-            const float4 a = rec[2 * s];                                         // a.x a.y a.z w.re
-            const float wim = reinterpret_cast<const float*>(rec)[8 * s + 4];   // w.im
-#pragma unroll
-            for (int v = 0; v < kV; ++v) {
-                const float p = fmaf(a.z, bz[v], fmaf(a.y, by[v], a.x * bx[v]));
-                float sn, cs;
-                if constexpr (MODE == kAccurate) {
-                    phasor_accurate(p, sn, cs);
-                } else if (v >= kV - NPOLY) {
-                    phasor_poly(p, sn, cs);
-                } else {
-                    phasor_mufu(p, sn, cs);
-                }
-                tr[v] = fmaf(a.w, cs, tr[v]);
-                tr[v] = fmaf(-wim, sn, tr[v]);
-                ti[v] = fmaf(a.w, sn, ti[v]);
-                ti[v] = fmaf(wim, cs, ti[v]);
-            }
-        }
+        if (strided)
+            accumulate_tile_strided<MODE>(rec, bx[0], by[0], bz[0], sx, sy, sz, tr, ti);
+        else
+            accumulate_tile<MODE, NPOLY>(rec, bx, by, bz, tr, ti);
 #pragma unroll
         for (int v = 0; v < kV; ++v) {
             sm.run[v][tid] += tr[v];
@@ -413,11 +500,11 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
         if (w == w_end - 1 || j == sch.n_tiles - 1) {
             // end of segment: whole block -> output, else -> this CTA's partial slot
             const bool whole = (seg_first_tile == 0) && (j == sch.n_tiles - 1);
-            const int64_t base = b * kTargetsPerBlock + threadIdx.x;
+            const int64_t base = b * kTargetsPerBlock + (int64_t)tid * kV;
             if (whole) {
 #pragma unroll
                 for (int v = 0; v < kV; ++v) {
-                    const int64_t t = base + (int64_t)v * kThreads;
+                    const int64_t t = base + v;
                     if (t < sch.n_targets) {
                         args.out_r[t] = sm.run[v][tid];
                         args.out_i[t] = sm.run[kV + v][tid];
@@ -429,8 +516,8 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
                 float* pi = pr + kTargetsPerBlock;
 #pragma unroll
                 for (int v = 0; v < kV; ++v) {
-                    pr[tid + v * kThreads] = sm.run[v][tid];
-                    pi[tid + v * kThreads] = sm.run[kV + v][tid];
+                    pr[tid * kV + v] = sm.run[v][tid];
+                    pi[tid * kV + v] = sm.run[kV + v][tid];
                 }
             }
         }

@@ -69,6 +69,7 @@ def test_rejects_negative_sizes(lib):
 
 def test_rejects_bad_mode(lib):
     assert call_fhd(lib, mode=7) == 1
+    assert call_fhd(lib, mode=4) == 1
 
 
 def test_rejects_null(lib):

@@ -21,7 +21,8 @@ from tests.gpu_helpers import (PSNR_FAST_DB, TOL_ACCURATE, TOL_FAST, gpu_fhd, gp
 
 pytestmark = pytest.mark.gpu
 
-ACC, FAST = 0, 1
+ACC, FAST, ACC_DIRECT, FAST_DIRECT = 0, 1, 2, 3
+ALL_MODES = [ACC, FAST, ACC_DIRECT, FAST_DIRECT]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,7 +39,7 @@ def _lib():
 
 def check(got, ref, mode, what):
     err = rel_l2(got, ref)
-    if mode == ACC:
+    if (mode & 1) == 0:
         assert err <= TOL_ACCURATE, f"{what}: accurate relL2 {err:.3e}"
     else:
         assert err <= TOL_FAST, f"{what}: fast relL2 {err:.3e}"
@@ -59,7 +60,7 @@ def test_fhd_random(N, M, mode):
     check(gpu_fhd(p, mode), ref, mode, f"F^H D N={N} M={M}")
 
 
-@pytest.mark.parametrize("mode", [ACC, FAST])
+@pytest.mark.parametrize("mode", ALL_MODES)
 def test_fhd_2d_grid(mode):
     p = random_problem(4500, 1500, kmax=16.0, seed=3, dims=2, coords="grid")
     assert np.all(p.z == 0)
@@ -94,7 +95,7 @@ def workload(i):
     return _cache[i]
 
 
-@pytest.mark.parametrize("mode", [ACC, FAST])
+@pytest.mark.parametrize("mode", ALL_MODES)
 def test_workload1_full(mode):
     p = workload(1)
     ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
@@ -107,7 +108,7 @@ def ref2():
     return oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
 
 
-@pytest.mark.parametrize("mode", [ACC, FAST])
+@pytest.mark.parametrize("mode", ALL_MODES)
 def test_workload2_full(mode, ref2):
     check(gpu_fhd(workload(2), mode), ref2, mode, "workload 2")
 
@@ -151,6 +152,58 @@ def test_workload5(mode):
     assert abs(q.real - nrm) <= (1e-4 if mode == ACC else 1e-2) * nrm
 
 
+# ------------------------------------------------------------ equal-spacing recurrence
+
+@pytest.mark.parametrize("N,M", [(4096, 1000), (5000, 777), (70000, 300)])
+@pytest.mark.parametrize("mode", ALL_MODES)
+def test_fhd_3d_grid_ragged(N, M, mode):
+    """First N voxels of a 3D grid: rows of equally spaced voxels (recurrence),
+    a ragged last row and a ragged last block."""
+    p = random_problem(N, M, kmax=32.0, seed=N + M, coords="grid")
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    check(gpu_fhd(p, mode), ref, mode, f"F^H D grid N={N} M={M}")
+
+
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_perturbed_grid_falls_back(mode):
+    """One voxel moved by one float32 ulp breaks the exact spacing of its row:
+    that warp evaluates pair by pair, the others use the recurrence; all match."""
+    p = random_problem(32768, 900, kmax=30.0, seed=5, coords="grid")  # a 32^3 grid
+    p.x = p.x.copy()
+    p.x[3001] = np.nextafter(p.x[3001], np.float32(1.0))
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    check(gpu_fhd(p, mode), ref, mode, "F^H D perturbed grid")
+
+
+def test_recurrence_and_direct_differ_but_both_match():
+    p = random_problem(32768, 2000, kmax=32.0, seed=6, coords="grid")  # a 32^3 grid: exact spacing
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    for fast in (0, 1):
+        a = gpu_fhd(p, fast)
+        b = gpu_fhd(p, fast | 2)
+        check(a, ref, fast, "recurrence")
+        check(b, ref, fast | 2, "direct")
+        assert not np.array_equal(a, b), "the recurrence path did not run"
+
+
+@pytest.mark.parametrize("mode", ALL_MODES)
+def test_fwd_radial_spokes(mode):
+    """F rho with samples along radial spokes: directions rounded to multiples of
+    2^-12 make every sample r*d exact in float32, so the samples of a spoke are
+    exactly equally spaced targets and take the recurrence."""
+    rng = np.random.default_rng(7)
+    d = rng.standard_normal((13, 3))
+    d /= np.linalg.norm(d, axis=1, keepdims=True)
+    d = np.round(d * 4096) / 4096
+    r = np.arange(256) - 128.0
+    k = (d[:, None, :] * r[None, :, None]).reshape(-1, 3).astype(np.float32)
+    assert np.array_equal(k.astype(np.float64), (d[:, None, :] * r[None, :, None]).reshape(-1, 3))
+    p = random_problem(3000, k.shape[0], kmax=1.0, seed=7, op="fwd")
+    p.kx, p.ky, p.kz = (np.ascontiguousarray(k[:, i]) for i in range(3))
+    ref = oracle.forward(p.x, p.y, p.z, p.rho_r + 1j * p.rho_i, p.kx, p.ky, p.kz)
+    check(gpu_fwd(p, mode), ref, mode, "F rho radial")
+
+
 # ------------------------------------------------------------ edge cases
 
 def test_empty_and_zero_sources():
@@ -173,8 +226,9 @@ def test_empty_and_zero_sources():
 
 
 @pytest.mark.parametrize("mode", [ACC, FAST])
-def test_deterministic(mode):
-    p = random_problem(30000, 5000, kmax=32.0, seed=21)
+@pytest.mark.parametrize("coords", ["uniform", "grid"])
+def test_deterministic(mode, coords):
+    p = random_problem(30000, 5000, kmax=32.0, seed=21, coords=coords)
     a = gpu_fhd(p, mode)
     b = gpu_fhd(p, mode)
     assert np.array_equal(a, b)
