@@ -15,17 +15,20 @@ e2e        the same metric through the public API with pinned HOST buffers:
            every step copies the inputs host->device, runs fhd_compute and
            copies rho back device->host, all inside the timed region.
 roofline   the gather kernel against its plain-ALU bound
-           SMs x clock x min(128 / n_fma, 16 / n_mufu, 128 / (n_fma + n_mufu))
-           pairs/s: 128 FMA-pipe lanes, 16 MUFU lanes and one warp instruction
-           issued per scheduler per clock, per SM; n_fma and n_mufu are the
-           algorithm's instructions per pair.  Pair by pair (direct): 7 and 2
-           (k.x, complex MAC; sin, cos).  Equal-spacing recurrence on the
-           benchmark's grid voxels, V = 8 targets per thread: per pair one
-           complex step (4, skipped for the first target) and two adds, plus per
-           (thread, sample) two phases (6) and D*exp(i theta_0) (4), and 4 MUFU
-           -> n_fma = 6 - 4/V + 10/V, n_mufu = 4/V.  Maximum SM clock.  The
-           kernel's duration comes from CUDA events recorded on its stream
-           around the gather and fix-up launches of every timed step.
+           SMs x clock x min(128 / n_fma, 16 / n_mufu, 128 / n_issue) pairs/s:
+           128 FP32 lanes, 16 MUFU lanes and 4 schedulers issuing one warp
+           instruction (32 lanes) per clock, per SM; n_fma, n_mufu and n_issue
+           are the algorithm's FP32 lane operations, MUFU operations and
+           instructions per pair.  Pair by pair (direct): 7, 2, 9 (k.x and the
+           complex MAC; sin, cos).  Equal-spacing recurrence on the benchmark's
+           grid voxels, V = 16 targets per thread, packed f32x2 arithmetic:
+           per target one packed add and (from the third target on) one packed
+           three-term step, plus per (thread, sample) the two phases (3 packed
+           instructions), D*exp(i theta_0) (4), its first step (4),
+           2 cos(theta_d) (1) and 4 MUFU -> n_fma = 4 - 4/V + 15/V,
+           n_mufu = 4/V, n_issue = 2 + 14/V.  Maximum SM clock.  The kernel's
+           duration comes from CUDA events recorded on its stream around the
+           gather and fix-up launches of every timed step.
 cpu_baseline  the fp64 CPU oracle on a bounded voxel sample of the same
            workload (test infrastructure; never used by the GPU path).
 
@@ -53,16 +56,28 @@ FLOP_PER_PAIR = 13
 FMA_LANES_PER_SM = 128   # fp32 FMA-pipe results per SM per clock
 MUFU_LANES_PER_SM = 16   # sin/cos results per SM per clock (measured on GB300)
 ISSUE_PER_SM = 128       # 4 schedulers x 1 warp instruction (32 lanes) per clock
-TARGETS_PER_THREAD = 8
+L2_BYTES = 129 * 1024 * 1024
+TARGETS_PER_THREAD = 16
 
 
 def per_pair_counts(path: str):
-    """(FMA-pipe, MUFU) instructions per pair of the algorithm on `path`."""
+    """(FP32 lane operations, MUFU operations, issued instructions) per pair of
+    the algorithm on `path` (all three count what the algorithm needs, not what
+    the compiler emits)."""
     if path == "direct":
-        return 7.0, 2.0          # k.x (1 FMUL + 2 FFMA) + complex MAC (4 FFMA); sin, cos
+        # k.x (1 FMUL + 2 FFMA) + complex MAC (4 FFMA); sin, cos
+        return 7.0, 2.0, 9.0
+    # recurrence, V targets per thread.  Per (thread, sample): the two phases
+    # as 3 packed instructions (6 lane operations), g_0 = D exp(i theta_0) (4),
+    # g_1 = g_0 u (4), 2 cos(theta_d) (1), 4 MUFU.  Per target: one packed add
+    # into its accumulator (2 lane operations), and from the third target on
+    # one packed three-term step (2 lane operations).
     V = TARGETS_PER_THREAD
-    return 6.0 - 4.0 / V + 10.0 / V, 4.0 / V
-L2_BYTES = 129 * 1024 * 1024
+    lanes = 4.0 - 4.0 / V + 15.0 / V
+    mufu = 4.0 / V
+    issue = (2.0 * V - 2.0 + 3.0 + 4.0 + 4.0 + 1.0 + 4.0) / V
+    return lanes, mufu, issue
+
 
 WORKLOAD_NAMES = {
     1: "2D 32x32 voxels x 2048 spiral samples, F^H D",
@@ -184,8 +199,8 @@ def load_workload(i: int):
 
 
 def peak_pairs_per_s(sms: int, mhz: float, path: str = "direct") -> float:
-    n_fma, n_mufu = per_pair_counts(path)
-    per_clk = min(FMA_LANES_PER_SM / n_fma, MUFU_LANES_PER_SM / n_mufu, ISSUE_PER_SM / (n_fma + n_mufu))
+    n_fma, n_mufu, n_issue = per_pair_counts(path)
+    per_clk = min(FMA_LANES_PER_SM / n_fma, MUFU_LANES_PER_SM / n_mufu, ISSUE_PER_SM / n_issue)
     return sms * per_clk * mhz * 1e6
 
 
@@ -391,7 +406,7 @@ def run_ours(args, world, rank, local):
     max_mhz = float(peaks.get("sm_max_mhz") or clk.get("sm_max_mhz") or 2070.0)
     peak = peak_pairs_per_s(sms, max_mhz, path)
     achieved = pairs / (gather_ms * 1e-3)
-    n_fma, n_mufu = per_pair_counts(path)
+    n_fma, n_mufu, n_issue = per_pair_counts(path)
     roof = {
         "bound": "alu",
         "achieved": FLOP_PER_PAIR * achieved / 1e12,
@@ -404,7 +419,7 @@ def run_ours(args, world, rank, local):
         "kernel_ms": gather_ms,
         "path": path,
         "peak_basis": (f"{sms} SMs x {max_mhz:.0f} MHz x min({FMA_LANES_PER_SM}/{n_fma:g}, "
-                       f"{MUFU_LANES_PER_SM}/{n_mufu:g}, {ISSUE_PER_SM}/{n_fma + n_mufu:g}) pairs/clk x "
+                       f"{MUFU_LANES_PER_SM}/{n_mufu:g}, {ISSUE_PER_SM}/{n_issue:g}) pairs/clk x "
                        f"{FLOP_PER_PAIR} flop/pair ({path} path)"),
         "direct_path_peak": FLOP_PER_PAIR * peak_pairs_per_s(sms, max_mhz, "direct") / 1e12,
     }

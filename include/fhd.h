@@ -51,7 +51,7 @@
  *            hardware sin/cos approximations, partly replaced by an FMA-pipe
  *            polynomial (relative L2 error below 1e-3).  Either may be OR-ed
  *            with FHD_MODE_DIRECT, see below.
- * Spacing    where a thread's 8 consecutive targets (voxels for F^H D,
+ * Spacing    where a thread's 16 consecutive targets (voxels for F^H D,
  *            samples for F rho) are exactly equally spaced, as the voxels of a
  *            regular image grid are, the kernel evaluates two phasors per
  *            (thread, source) and reaches the other targets by the recurrence
@@ -209,7 +209,7 @@ fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *threads,
  * problems return FHD_ERR_TOO_LARGE before anything is launched; N is not
  * limited.
  *
- * Memory: every GPU that loads the library holds the array (about 16 MiB)
+ * Memory: every GPU that loads the library holds the array (about 19 MiB)
  * until the process exits.  The first call on a device, with that device
  * current, looks up the array's device address (cudaGetSymbolAddress) and
  * caches it; make that first call before any stream capture begins.
@@ -222,9 +222,9 @@ fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *threads,
  * stream.  fhd_workspace_status() does not apply to this entry point.
  */
 #define FHD_NOALLOC_MAX_SAMPLES 131072
-#define FHD_NOALLOC_MAX_CTAS 192
+#define FHD_NOALLOC_MAX_CTAS 160
 #define FHD_NOALLOC_SCRATCH_BYTES (512 + (size_t)FHD_NOALLOC_MAX_SAMPLES * 32 + \
-                                   (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * 4096 * 4)
+                                   (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * 6144 * 4)
 fhd_status fhd_compute_noalloc(int64_t M, const float *kx, const float *ky, const float *kz,
                                const float *Dr, const float *Di,
                                int64_t N, const float *x, const float *y, const float *z,

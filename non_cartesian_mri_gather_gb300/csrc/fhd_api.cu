@@ -406,8 +406,9 @@ int fhd_version(void) { return kVersion; }
 // partial slot the fix-up reads is written by its CTA first).
 namespace {
 
-// FHD_NOALLOC_SCRATCH_BYTES is the size for the default launch shape; builds
-// with other shape constants size the array for their own layout.
+// FHD_NOALLOC_SCRATCH_BYTES is the size for the default launch shape (6144
+// targets per block); builds with other shape constants size the array for
+// their own layout.
 constexpr size_t kNoAllocLayoutBytes = kHeaderBytes + (size_t)FHD_NOALLOC_MAX_SAMPLES * kRecordBytes + kWsAlign +
                                        (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * kTargetsPerBlock * sizeof(float);
 constexpr size_t kNoAllocScratchBytes =

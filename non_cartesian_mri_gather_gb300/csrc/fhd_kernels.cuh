@@ -15,8 +15,9 @@
 // Pipeline of one call:
 //   1. pack_sources   - loop fission / per-source precompute (section 17.3.2):
 //                       SoA source arrays -> 32-byte AoS records
-//                       {a.x, a.y, a.z, w.re, w.im, 0, 0, 0}, padded with
-//                       zero-weight records to a whole number of tiles.  The
+//                       {A.x, A.x, A.y, A.y, A.z, A.z, w.re, w.im} (A the
+//                       scaled source coordinates), padded with zero-weight
+//                       records to a whole number of tiles.  The
 //                       array-of-structures record follows the mtuann notes'
 //                       step 4 and the SampleChunk struct of section 17.3.4.
 //   2. gather_kernel  - persistent CTAs; each owns an equal contiguous range
@@ -25,9 +26,11 @@
 //                       memory ring with non-multicast bulk async copies
 //                       completing on mbarriers; consumer warps read each
 //                       record as a broadcast (the role the constant cache
-//                       plays in section 17.3.4), keep V targets' coordinates
-//                       and accumulators in registers (privatisation, section
-//                       17.3.3) and write every output once.
+//                       plays in section 17.3.4), keep per-tile accumulators
+//                       of kV consecutive targets in registers (privatisation,
+//                       section 17.3.3) and write every output once.  Equally
+//                       spaced targets take a recurrence instead of a sin/cos
+//                       per pair (accumulate_tile_strided).
 //   3. fixup_kernel   - target blocks whose source range was split between
 //                       CTAs are summed from per-CTA partials in a fixed
 //                       order (no atomics, bit-reproducible).
@@ -47,10 +50,10 @@ namespace fhd {
 // ---------------------------------------------------------------- shape
 // Compile-time launch shape (overridable with -D for tuning builds).
 #ifndef FHD_THREADS
-#define FHD_THREADS 512
+#define FHD_THREADS 384
 #endif
 #ifndef FHD_V
-#define FHD_V 8
+#define FHD_V 16
 #endif
 #ifndef FHD_TILE
 #define FHD_TILE 128
@@ -65,7 +68,7 @@ namespace fhd {
 #define FHD_FAST_POLY_SLOTS 1
 #endif
 #ifndef FHD_UNROLL
-#define FHD_UNROLL 2
+#define FHD_UNROLL 4
 #endif
 
 constexpr int kThreads = FHD_THREADS;    // consumer threads per CTA
@@ -87,8 +90,12 @@ constexpr uint32_t kStatusProducerTimeout = 2u;
 constexpr uint32_t kStatusDrainTimeout = 4u;
 
 enum Mode : int { kAccurate = 0, kFast = 1 };
-constexpr int kFastPolySlots = FHD_FAST_POLY_SLOTS;  // of kV: share of sin/cos moved to the FMA pipe
-static_assert(kFastPolySlots >= 0 && kFastPolySlots <= kV, "bad polynomial split");
+// The pair-by-pair path walks a thread's kV targets in groups of kDirectGroup
+// (coordinates of one group in registers at a time).
+constexpr int kDirectGroup = kV < 8 ? kV : 8;
+static_assert(kV % kDirectGroup == 0, "kV must be a multiple of the direct-path group");
+constexpr int kFastPolySlots = FHD_FAST_POLY_SLOTS;  // of kDirectGroup: share of sin/cos on the FMA pipe
+static_assert(kFastPolySlots >= 0 && kFastPolySlots <= kDirectGroup, "bad polynomial split");
 
 
 // Static schedule shared by the gather and fix-up kernels (and by the
@@ -252,7 +259,9 @@ __device__ __forceinline__ void phasor_poly(float P, float& s, float& c) {
 }
 
 // ---------------------------------------------------------------- pack
-// Source records {scale*a.x, scale*a.y, scale*a.z, w.re, w.im, 0, 0, 0};
+// Source records {A.x, A.x, A.y, A.y, A.z, A.z, w.re, w.im} with A = scale*a:
+// each coordinate twice, so one 16-byte load gives (A.x, A.x, A.y, A.y) as the
+// packed pairs the recurrence multiplies by (x0, dx) and (y0, dy);
 // scale is +-1 (accurate mode, phase in cycles) or +-2 pi (fast mode, phase
 // in radians), negative for the forward sum.
 // Records n..n_padded-1 are zero (weight 0, so they add exactly 0).
@@ -269,8 +278,9 @@ __global__ void pack_sources(const float* __restrict__ ax, const float* __restri
         float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f);
         float4 r1 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < n) {
-            r0 = make_float4(scale * ax[i], scale * ay[i], scale * az[i], wr[i]);
-            r1.x = wi[i];
+            const float X = scale * ax[i], Y = scale * ay[i], Z = scale * az[i];
+            r0 = make_float4(X, X, Y, Y);
+            r1 = make_float4(Z, Z, wr[i], wi[i]);
         }
         out[2 * i] = r0;
         out[2 * i + 1] = r1;
@@ -285,6 +295,11 @@ struct __align__(16) GatherSmem {
     // once per tile, so keeping them here instead of in registers frees
     // 2*kV registers per thread for more resident warps.
     float run[2 * kV][kThreads];
+    // Target coordinates of the current segment, one private column per
+    // consumer thread (rows: x, y, z of each of the kV targets).  The
+    // pair-by-pair path re-reads kDirectGroup targets' coordinates per tile;
+    // the recurrence needs only b_0 and d, which stay in registers.
+    float coord[3 * kV][kThreads];
     uint64_t full[kStages];
     uint64_t empty[kStages];
 };
@@ -294,33 +309,66 @@ struct __align__(16) GatherSmem {
 // thread's kV targets.  In fast mode the last NPOLY register slots take the
 // FMA-pipe polynomial, the others the MUFU pipe.
 template <int MODE, int NPOLY>
-__device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, const float (&bx)[kV],
-                                                const float (&by)[kV], const float (&bz)[kV], float (&tr)[kV],
-                                                float (&ti)[kV]) {
+__device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, const float (*coord)[kThreads],
+                                                int tid, float (&tr)[kV], float (&ti)[kV]) {
 #pragma unroll
     for (int v = 0; v < kV; ++v) {
         tr[v] = 0.f;
         ti[v] = 0.f;
     }
-#pragma unroll kUnroll
-    for (int s = 0; s < kTile; ++s) {
-        const float4 a = rec[2 * s];                                         // a.x a.y a.z w.re
-        const float wim = reinterpret_cast<const float*>(rec)[8 * s + 4];   // w.im
+#pragma unroll 1
+    for (int g = 0; g < kV; g += kDirectGroup) {
+        float bx[kDirectGroup], by[kDirectGroup], bz[kDirectGroup];
 #pragma unroll
-        for (int v = 0; v < kV; ++v) {
-            const float p = fmaf(a.z, bz[v], fmaf(a.y, by[v], a.x * bx[v]));
-            float sn, cs;
-            if constexpr (MODE == kAccurate) {
-                phasor_accurate(p, sn, cs);
-            } else if (v >= kV - NPOLY) {
-                phasor_poly(p, sn, cs);
-            } else {
-                phasor_mufu(p, sn, cs);
+        for (int v = 0; v < kDirectGroup; ++v) {
+            bx[v] = coord[g + v][tid];
+            by[v] = coord[kV + g + v][tid];
+            bz[v] = coord[2 * kV + g + v][tid];
+        }
+        float gr[kDirectGroup], gi[kDirectGroup];
+#pragma unroll
+        for (int v = 0; v < kDirectGroup; ++v) {
+            gr[v] = 0.f;
+            gi[v] = 0.f;
+        }
+#pragma unroll kUnroll
+        for (int s = 0; s < kTile; ++s) {
+            const float4 r0 = rec[2 * s];      // A.x A.x A.y A.y
+            const float4 r1 = rec[2 * s + 1];  // A.z A.z w.re w.im
+#pragma unroll
+            for (int v = 0; v < kDirectGroup; ++v) {
+                const float p = fmaf(r1.x, bz[v], fmaf(r0.z, by[v], r0.x * bx[v]));
+                float sn, cs;
+                if constexpr (MODE == kAccurate) {
+                    phasor_accurate(p, sn, cs);
+                } else if (v >= kDirectGroup - NPOLY) {
+                    phasor_poly(p, sn, cs);
+                } else {
+                    phasor_mufu(p, sn, cs);
+                }
+                gr[v] = fmaf(r1.z, cs, gr[v]);
+                gr[v] = fmaf(-r1.w, sn, gr[v]);
+                gi[v] = fmaf(r1.z, sn, gi[v]);
+                gi[v] = fmaf(r1.w, cs, gi[v]);
             }
-            tr[v] = fmaf(a.w, cs, tr[v]);
-            tr[v] = fmaf(-wim, sn, tr[v]);
-            ti[v] = fmaf(a.w, sn, ti[v]);
-            ti[v] = fmaf(wim, cs, ti[v]);
+        }
+#pragma unroll
+        for (int v = 0; v < kDirectGroup; ++v) {
+            if (g == 0) {  // the group loop is not unrolled: select into fixed registers
+                tr[v] = gr[v];
+                ti[v] = gi[v];
+            }
+        }
+        if constexpr (kV > kDirectGroup) {
+#pragma unroll
+            for (int gg = kDirectGroup; gg < kV; gg += kDirectGroup)
+                if (g == gg) {
+#pragma unroll
+                    for (int v = 0; v < kDirectGroup; ++v) {
+                        tr[gg + v] = gr[v];
+                        ti[gg + v] = gi[v];
+                    }
+                }
         }
     }
 }
@@ -332,21 +380,65 @@ __device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, 
 // complex multiply f *= w (4 FMA-pipe instructions) and two adds into its
 // accumulators, instead of a phase and a sin/cos per pair.  Voxels of a
 // regular image grid, and samples along a radial spoke, are equally spaced.
+// Packed pairs of float32 (low = first, high = second) for the sm_100-family
+// f32x2 instructions: one instruction does two fp32 operations, so the
+// recurrence below spends one issue slot per target per operation.
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(f2_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+    f2_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+    f2_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+    f2_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Sign of the stored accumulator of target v in the recurrence below.
+__host__ __device__ constexpr bool strided_negated(int v) { return (v & 2) != 0; }
+
+// Equal-spacing recurrence.  When a thread's kV consecutive targets satisfy
+// b_v = b_0 + v*d exactly, exp(i 2 pi a.b_v) = exp(i 2 pi a.b_0) * u^v with
+// u = exp(i 2 pi a.d).  Per source the thread evaluates two phasors (b_0 and
+// d, phases formed as packed pairs) and g_0 = w_s exp(i 2 pi a.b_0),
+// g_1 = g_0 u.  The real and imaginary parts of g_v = g_0 u^v each follow
+// g_{v+1} = 2 cos(theta_d) g_v - g_{v-1} (u + 1/u = 2 cos theta_d for
+// |u| = 1); its fp32 error grows at most like eps * v^2 / 2.  With the signs
+// s_v = (+, +, -, -, ...) the scaled terms e_v = s_v g_v obey
+// e_{v+1} = -+2 cos(theta_d) e_v + e_{v-1} (the coefficient alternating,
+// -2 cos first), so each target costs one packed FMA for the step and one
+// packed add into its accumulator, which holds s_v times the sum.  Voxels of a
+// regular image grid, and samples along a radial spoke, are equally spaced.
 template <int MODE>
 __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict__ rec, float x0, float y0,
-                                                        float z0, float dx, float dy, float dz, float (&tr)[kV],
-                                                        float (&ti)[kV]) {
+                                                        float z0, float dx, float dy, float dz, f2_t (&acc)[kV]) {
 #pragma unroll
-    for (int v = 0; v < kV; ++v) {
-        tr[v] = 0.f;
-        ti[v] = 0.f;
-    }
+    for (int v = 0; v < kV; ++v) acc[v] = 0ull;  // +0.0f in both halves
+    const f2_t bx = f2_pack(x0, dx), by = f2_pack(y0, dy), bz = f2_pack(z0, dz);
 #pragma unroll kUnroll
     for (int s = 0; s < kTile; ++s) {
-        const float4 a = rec[2 * s];                                         // a.x a.y a.z w.re
-        const float wim = reinterpret_cast<const float*>(rec)[8 * s + 4];   // w.im
-        const float p0 = fmaf(a.z, z0, fmaf(a.y, y0, a.x * x0));
-        const float pd = fmaf(a.z, dz, fmaf(a.y, dy, a.x * dx));
+        const float4 r0 = rec[2 * s];      // A.x A.x A.y A.y
+        const float4 r1 = rec[2 * s + 1];  // A.z A.z w.re w.im
+        // (p0, pd) = A.b_0, A.d as one packed pair
+        const f2_t ph = f2_fma(f2_pack(r1.x, r1.y), bz,
+                               f2_fma(f2_pack(r0.z, r0.w), by, f2_mul(f2_pack(r0.x, r0.y), bx)));
+        float p0, pd;
+        f2_unpack(ph, p0, pd);
         float s0, c0, sw, cw;
         if constexpr (MODE == kAccurate) {
             phasor_accurate(p0, s0, c0);
@@ -355,17 +447,22 @@ __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict
             phasor_mufu(p0, s0, c0);
             phasor_mufu(pd, sw, cw);
         }
-        float fr = fmaf(a.w, c0, -wim * s0);  // f = w_s * exp(i 2 pi a.b_0)
-        float fi = fmaf(a.w, s0, wim * c0);
+        const float fr = fmaf(r1.z, c0, -r1.w * s0);  // g_0 = w_s * exp(i 2 pi a.b_0)
+        const float fi = fmaf(r1.z, s0, r1.w * c0);
+        const float gr = fmaf(fr, cw, -fi * sw);      // g_1 = g_0 u
+        const float gi = fmaf(fr, sw, fi * cw);
+        const float c2 = cw + cw;
+        const f2_t kpos = f2_pack(c2, c2), kneg = f2_pack(-c2, -c2);
+        f2_t em = f2_pack(fr, fi);  // e_{v-1}
+        f2_t e = f2_pack(gr, gi);   // e_v
+        acc[0] = f2_add(acc[0], em);
+        acc[1] = f2_add(acc[1], e);
 #pragma unroll
-        for (int v = 0; v < kV; ++v) {
-            tr[v] += fr;
-            ti[v] += fi;
-            if (v + 1 < kV) {
-                const float nr = fmaf(fr, cw, -fi * sw);  // f *= exp(i 2 pi a.d)
-                fi = fmaf(fr, sw, fi * cw);
-                fr = nr;
-            }
+        for (int v = 1; v + 1 < kV; ++v) {
+            const f2_t en = f2_fma((v & 1) ? kneg : kpos, e, em);  // e_{v+1}
+            em = e;
+            e = en;
+            acc[v + 1] = f2_add(acc[v + 1], e);
         }
     }
 }
@@ -444,7 +541,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
 
     // ---------------------------------------------------- consumer warps
     // Thread tid owns the kV consecutive targets b*kTargetsPerBlock + tid*kV + v.
-    float bx[kV], by[kV], bz[kV];
+    float x0 = 0.f, y0 = 0.f, z0 = 0.f;  // first target of the thread (strided path)
     float sx = 0.f, sy = 0.f, sz = 0.f;  // target spacing of the strided path
     bool strided = false;                // warp-uniform
     const int tid = threadIdx.x;
@@ -458,6 +555,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
             // new segment: this CTA's range enters target block b
             seg_first_tile = j;
             const int64_t base = b * kTargetsPerBlock + (int64_t)tid * kV;
+            float bx[kV], by[kV], bz[kV];
 #pragma unroll
             for (int v = 0; v < kV; ++v) {
                 const int64_t t = base + v;
@@ -465,9 +563,15 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
                 bx[v] = in ? args.tx[t] : 0.f;
                 by[v] = in ? args.ty[t] : 0.f;
                 bz[v] = in ? args.tz[t] : 0.f;
+                sm.coord[v][tid] = bx[v];
+                sm.coord[kV + v][tid] = by[v];
+                sm.coord[2 * kV + v][tid] = bz[v];
                 sm.run[v][tid] = 0.f;
                 sm.run[kV + v][tid] = 0.f;
             }
+            x0 = bx[0];
+            y0 = by[0];
+            z0 = bz[0];
             const int n_in = (int)(sch.n_targets - base < kV ? (sch.n_targets - base > 0 ? sch.n_targets - base : 0)
                                                              : kV);
             const bool spaced = equally_spaced(bx, n_in, sx) && equally_spaced(by, n_in, sy) &&
@@ -483,16 +587,30 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
         // Two-level accumulation: a fresh accumulator per tile, folded into the
         // running sum once per tile, keeps fp32 rounding growth at
         // O(sqrt(kTile) + sqrt(M / kTile)) instead of O(sqrt(M)).
-        float tr[kV], ti[kV];
         const float4* rec = &sm.ring[st][0];
-        if (strided)
-            accumulate_tile_strided<MODE>(rec, bx[0], by[0], bz[0], sx, sy, sz, tr, ti);
-        else
-            accumulate_tile<MODE, NPOLY>(rec, bx, by, bz, tr, ti);
+        if (strided) {
+            f2_t acc[kV];
+            accumulate_tile_strided<MODE>(rec, x0, y0, z0, sx, sy, sz, acc);
 #pragma unroll
-        for (int v = 0; v < kV; ++v) {
-            sm.run[v][tid] += tr[v];
-            sm.run[kV + v][tid] += ti[v];
+            for (int v = 0; v < kV; ++v) {
+                float re, im;
+                f2_unpack(acc[v], re, im);
+                if (strided_negated(v)) {
+                    sm.run[v][tid] -= re;
+                    sm.run[kV + v][tid] -= im;
+                } else {
+                    sm.run[v][tid] += re;
+                    sm.run[kV + v][tid] += im;
+                }
+            }
+        } else {
+            float tr[kV], ti[kV];
+            accumulate_tile<MODE, NPOLY>(rec, sm.coord, tid, tr, ti);
+#pragma unroll
+            for (int v = 0; v < kV; ++v) {
+                sm.run[v][tid] += tr[v];
+                sm.run[kV + v][tid] += ti[v];
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[st]);

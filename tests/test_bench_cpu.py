@@ -1,0 +1,78 @@
+"""bench.py host logic without a GPU: argument defaults, the roofline
+arithmetic, the reference arm on the small workload, and the multi-process
+reduction (max over ranks, barrier) on two gloo ranks."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_defaults(monkeypatch):
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse()
+    assert (a.gpus, a.steps, a.warmup, a.impl, a.workload, a.mode) == (1, 5, 3, "ours", 4, "fast")
+    assert a.warmup >= 3
+
+
+def test_roofline_counts():
+    # pair by pair: the MUFU pipe binds, 16 / 2 = 8 pairs per SM per clock
+    assert bench.per_pair_counts("direct") == (7.0, 2.0, 9.0)
+    assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct") - 152 * 8 * 2070e6) < 1
+    lanes, mufu, issue = bench.per_pair_counts("recurrence")
+    V = bench.TARGETS_PER_THREAD
+    assert abs(lanes - (4 - 4 / V + 15 / V)) < 1e-12 and abs(mufu - 4 / V) < 1e-12
+    assert abs(issue - (2 + 14 / V)) < 1e-12
+    # with V = 16 the FP32 lanes bind
+    assert abs(bench.peak_pairs_per_s(152, 2070.0, "recurrence") - 152 * (128 / lanes) * 2070e6) < 1
+
+
+def test_profiled_traffic_is_guarded():
+    assert bench.profiled_traffic(2, "fast") is None
+    assert bench.profiled_traffic(4, "accurate") is None
+    v = bench.profiled_traffic(4, "fast")
+    assert v is None or v > 0
+
+
+def test_reference_arm_runs(tmp_path):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "1",
+                        "--steps", "1", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "pairs/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+
+    sys.path.insert(0, ROOT)
+    import bench as b
+
+    w, r, _ = b.dist_init()
+    b.barrier(w)
+    m = b.max_over_ranks(10.0 + r, w)
+    with open(os.path.join(out, f"r{r}.txt"), "w") as f:
+        f.write(repr(m))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo(tmp_path):
+    import socket
+
+    import torch.multiprocessing as mp
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    mp.start_processes(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, start_method="spawn", join=True)
+    vals = [float(open(tmp_path / f"r{i}.txt").read()) for i in range(2)]
+    assert vals == [11.0, 11.0]
