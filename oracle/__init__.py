@@ -18,7 +18,10 @@ rho_n equation; section 17.2 for the forward operator F):
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` (closed forms,
 an FFT identity, Hermitian symmetry, the adjoint identity, brute force), and
-``tests/test_oracle_mutants.py`` shows the pins catch planted mistakes.
+``tests/test_oracle_mutants.py`` shows the pins catch planted mistakes.  The
+conjugate-gradient loop ``cg`` (plain numpy on these operators) is pinned by
+``tests/test_oracle_cg.py``: one-step convergence on a full Cartesian set, a
+dense numpy solve, and the monotone energy-norm error.
 """
 from __future__ import annotations
 
@@ -151,3 +154,44 @@ def forward(x, y, z, rho, kx, ky, kz) -> np.ndarray:
 
 def normal(x, y, z, rho, kx, ky, kz, **kw) -> np.ndarray:
     return get().normal(x, y, z, rho, kx, ky, kz, **kw)
+
+
+def cg(kx, ky, kz, D, x, y, z, lam: float = 0.0, max_iter: int = 10, tol: float = 0.0, orc=None,
+       _mutant: int = 0):
+    """Conjugate gradients on (F^H F + lam I) rho = F^H D, in the order of the
+    host loop of "Case study - iterative MRI reconstruction", section 17.3.6:
+
+        b = F^H D;  rho = 0;  r = b;  p = b;  rs_old = <r, r>
+        repeat max_iter times:
+            Ap = (F^H F + lam I) p
+            alpha = rs_old / <p, Ap>
+            rho += alpha p;  r -= alpha Ap
+            rs_new = <r, r>;  stop if rs_new < tol
+            p = r + (rs_new / rs_old) p;  rs_old = rs_new
+
+    (the page's loop has lam = 0; the Tikhonov term lam I is the plainest
+    reading of its regulariser R(rho) = ||rho||^2).  <a, b> = sum conj(a) b.
+    Returns (rho, iterations, [rs after each iteration]).  `_mutant` plants a
+    mistake for the test-suite's mutation checks (0: none).
+    """
+    orc = orc or get()
+    b = orc.adjoint(kx, ky, kz, D, x, y, z)
+    rho = np.zeros_like(b)
+    r = b.copy()
+    p = b.copy()
+    rs_old = float(np.vdot(r, r).real)
+    hist = []
+    it = 0
+    for it in range(1, max_iter + 1):
+        Ap = orc.normal(x, y, z, p, kx, ky, kz) + (0.0 if _mutant == 1 else lam) * p
+        alpha = rs_old / float(np.vdot(p, Ap).real)
+        rho = rho + alpha * p
+        r = r - alpha * Ap
+        rs_new = float(np.vdot(r, r).real)
+        hist.append(rs_new)
+        if rs_new < tol:
+            break
+        beta = (rs_old / rs_new) if _mutant == 2 else (rs_new / rs_old)
+        p = r + beta * p
+        rs_old = rs_new
+    return rho, it, hist
