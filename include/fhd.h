@@ -69,6 +69,13 @@
 #include <stddef.h>
 #include <stdint.h>
 
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define FHD_API __attribute__((visibility("default")))
+#else
+#define FHD_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -108,7 +115,7 @@ typedef enum {
  * invalid op, negative sizes or an unknown device.  The same workspace may be
  * reused by later calls on the same stream.
  */
-size_t fhd_workspace_bytes(fhd_op op, int64_t N, int64_t M, int device);
+FHD_API size_t fhd_workspace_bytes(fhd_op op, int64_t N, int64_t M, int device);
 
 /*
  * Adjoint non-uniform Fourier sum F^H D (section 17.3, the rho_n equation):
@@ -119,7 +126,7 @@ size_t fhd_workspace_bytes(fhd_op op, int64_t N, int64_t M, int device);
  * voxels x, y, z (length N each).  Outputs: rho_r, rho_i (length N).
  * M == 0 writes zeros; N == 0 does nothing (pointers may then be NULL).
  */
-fhd_status fhd_compute(int64_t M, const float *kx, const float *ky, const float *kz,
+FHD_API fhd_status fhd_compute(int64_t M, const float *kx, const float *ky, const float *kz,
                        const float *Dr, const float *Di,
                        int64_t N, const float *x, const float *y, const float *z,
                        float *rho_r, float *rho_i, fhd_mode mode,
@@ -134,7 +141,7 @@ typedef struct CUevent_st *fhd_event_t;
  * (the sample-pack kernel runs before `gather_start`).  Either event may be
  * NULL.  Used to time the dominant kernel inside a larger timed region.
  */
-fhd_status fhd_compute_profiled(int64_t M, const float *kx, const float *ky, const float *kz,
+FHD_API fhd_status fhd_compute_profiled(int64_t M, const float *kx, const float *ky, const float *kz,
                                 const float *Dr, const float *Di,
                                 int64_t N, const float *x, const float *y, const float *z,
                                 float *rho_r, float *rho_i, fhd_mode mode,
@@ -151,7 +158,7 @@ fhd_status fhd_compute_profiled(int64_t M, const float *kx, const float *ky, con
  * and M sample coordinates kx, ky, kz.  Outputs: Dr, Di (length M).
  * N == 0 writes zeros; M == 0 does nothing.
  */
-fhd_status fwd_compute(int64_t N, const float *x, const float *y, const float *z,
+FHD_API fhd_status fwd_compute(int64_t N, const float *x, const float *y, const float *z,
                        const float *rho_r, const float *rho_i,
                        int64_t M, const float *kx, const float *ky, const float *kz,
                        float *Dr, float *Di, fhd_mode mode,
@@ -164,7 +171,7 @@ fhd_status fwd_compute(int64_t N, const float *x, const float *y, const float *z
  * Inputs: N voxels x, y, z, rho_r, rho_i and M sample coordinates.
  * Outputs: out_r, out_i (length N).  M == 0 writes zeros; N == 0 does nothing.
  */
-fhd_status fhfrho_apply(int64_t N, const float *x, const float *y, const float *z,
+FHD_API fhd_status fhfrho_apply(int64_t N, const float *x, const float *y, const float *z,
                         const float *rho_r, const float *rho_i,
                         int64_t M, const float *kx, const float *ky, const float *kz,
                         float *out_r, float *out_i, fhd_mode mode,
@@ -175,10 +182,10 @@ fhd_status fhfrho_apply(int64_t N, const float *x, const float *y, const float *
  * reads the word and returns FHD_OK or FHD_ERR_TIMEOUT (FHD_ERR_CUDA if the
  * read fails, FHD_ERR_INVALID_VALUE for a NULL workspace).
  */
-fhd_status fhd_workspace_status(const void *workspace, fhd_stream_t stream);
+FHD_API fhd_status fhd_workspace_status(const void *workspace, fhd_stream_t stream);
 
 /* Static, NUL-terminated description of a status code. */
-const char *fhd_status_string(fhd_status status);
+FHD_API const char *fhd_status_string(fhd_status status);
 
 /*
  * Launch shape the sums use on `device`: CTAs per launch (one persistent CTA
@@ -186,7 +193,7 @@ const char *fhd_status_string(fhd_status status);
  * per staged tile and pipeline stages.  Any pointer may be NULL.  Returns
  * FHD_ERR_INVALID_VALUE for an unknown device.
  */
-fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *threads,
+FHD_API fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *threads,
                             int *targets_per_thread, int *tile_sources, int *stages);
 
 /*
@@ -225,13 +232,56 @@ fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *threads,
 #define FHD_NOALLOC_MAX_CTAS 160
 #define FHD_NOALLOC_SCRATCH_BYTES (512 + (size_t)FHD_NOALLOC_MAX_SAMPLES * 32 + \
                                    (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * 6144 * 4)
-fhd_status fhd_compute_noalloc(int64_t M, const float *kx, const float *ky, const float *kz,
+FHD_API fhd_status fhd_compute_noalloc(int64_t M, const float *kx, const float *ky, const float *kz,
                                const float *Dr, const float *Di,
                                int64_t N, const float *x, const float *y, const float *z,
                                float *rho_r, float *rho_i, fhd_mode mode, fhd_stream_t stream);
 
+/*
+ * Conjugate-gradient reconstruction: solves (F^H F + lambda I) rho = F^H D for
+ * rho, starting from rho = 0, with the loop of the host skeleton in section
+ * 17.3.6 of the case study:
+ *
+ *     b = F^H D;  r = p = b;  rs_old = <r, r>
+ *     repeat max_iter times:
+ *         Ap = (F^H F + lambda I) p;  alpha = rs_old / <p, Ap>
+ *         rho += alpha p;  r -= alpha Ap;  rs_new = <r, r>
+ *         stop if rs_new < tol;  p = r + (rs_new / rs_old) p;  rs_old = rs_new
+ *
+ * lambda >= 0 adds the Tikhonov term lambda I (the plainest reading of the
+ * regulariser R(rho) of section 17.2; lambda = 0 is the page's loop).  tol is
+ * compared with rs_new = ||r||^2, as on the page (absolute, squared).
+ * <a, b> = sum conj(a) b, accumulated in fp64 in a fixed order.
+ *
+ * Inputs and outputs as fhd_compute (M samples kx, ky, kz, Dr, Di; N voxels
+ * x, y, z; result rho_r, rho_i, overwritten).  The workspace (size from
+ * fhd_cg_workspace_bytes) holds r, p, A p, F p and the scalars.  Every
+ * iteration is enqueued on `stream` without a host synchronisation: the
+ * scalars stay on the device, and once rs_new < tol every later kernel of
+ * the call returns immediately.  fhd_cg_info() reports the outcome.
+ * Errors as for fhd_compute; also FHD_ERR_INVALID_VALUE for lambda < 0,
+ * max_iter < 0 or tol < 0.
+ */
+FHD_API size_t fhd_cg_workspace_bytes(int64_t N, int64_t M, int device);
+FHD_API fhd_status fhd_cg_solve(int64_t M, const float *kx, const float *ky, const float *kz,
+                                const float *Dr, const float *Di,
+                                int64_t N, const float *x, const float *y, const float *z,
+                                float lambda, int max_iter, double tol,
+                                float *rho_r, float *rho_i, fhd_mode mode,
+                                void *workspace, size_t workspace_bytes, fhd_stream_t stream);
+
+/*
+ * Outcome of the last fhd_cg_solve on `workspace`: synchronises `stream`, then
+ * reports the completed iterations, the last rs_new = ||r||^2 and whether the
+ * loop stopped early (1: rs_new < tol, 0: ran max_iter iterations, -1: stopped
+ * because <p, A p> was not positive).  Any output pointer may be NULL.
+ * Returns FHD_ERR_TIMEOUT if a kernel's bounded wait expired during the call.
+ */
+FHD_API fhd_status fhd_cg_info(const void *workspace, fhd_stream_t stream, int *iterations, double *residual,
+                               int *stopped);
+
 /* Library version as major*10000 + minor*100 + patch. */
-int fhd_version(void);
+FHD_API int fhd_version(void);
 
 #ifdef __cplusplus
 }

@@ -24,7 +24,7 @@ extern "C" {
  * leaves.  fhd_workspace_status() then returns FHD_ERR_TIMEOUT and the CUDA
  * context stays usable.  Output contents are unspecified after a timeout.
  */
-fhd_status fhd_test_compute_skip_tile(int64_t M, const float *kx, const float *ky, const float *kz,
+FHD_API fhd_status fhd_test_compute_skip_tile(int64_t M, const float *kx, const float *ky, const float *kz,
                                       const float *Dr, const float *Di,
                                       int64_t N, const float *x, const float *y, const float *z,
                                       float *rho_r, float *rho_i, fhd_mode mode,
@@ -41,7 +41,7 @@ fhd_status fhd_test_compute_skip_tile(int64_t M, const float *kx, const float *k
  * otherwise a positive code naming the first violated property.  Makes no
  * CUDA call.
  */
-int fhd_test_schedule(int64_t n_targets, int64_t n_sources, int ctas);
+FHD_API int fhd_test_schedule(int64_t n_targets, int64_t n_sources, int ctas);
 
 /*
  * The per-array check every operator applies before launching: `p` must be
@@ -50,7 +50,7 @@ int fhd_test_schedule(int64_t n_targets, int64_t n_sources, int ctas);
  * FHD_ERR_INVALID_VALUE, FHD_ERR_MISALIGNED or FHD_ERR_RANGE; launches
  * nothing, so a rejected pointer is never dereferenced.
  */
-fhd_status fhd_test_check_array(const void *p, size_t bytes, int device);
+FHD_API fhd_status fhd_test_check_array(const void *p, size_t bytes, int device);
 
 #ifdef __cplusplus
 }

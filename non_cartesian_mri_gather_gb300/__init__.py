@@ -43,6 +43,8 @@ __all__ = [
     "fhd_launch_shape",
     "fhd_version",
     "fhd_compute_noalloc",
+    "fhd_cg_solve",
+    "CgWorkspace",
     "Workspace",
 ]
 
@@ -85,6 +87,10 @@ SIGNATURES = {
     "fhd_launch_shape": (_int, [_int, _int, _vp, _vp, _vp, _vp, _vp]),
     "fhd_version": (_int, []),
     "fhd_compute_noalloc": (_int, [_i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp]),
+    "fhd_cg_workspace_bytes": (_sz, [_i64, _i64, _int]),
+    "fhd_cg_solve": (_int, [_i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, ctypes.c_float, _int,
+                            ctypes.c_double, _vp, _vp, _int, _vp, _sz, _vp]),
+    "fhd_cg_info": (_int, [_vp, _vp, _vp, _vp, _vp]),
     "fhd_test_compute_skip_tile": (_int, [_i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp,
                                           _sz, _vp, _i64]),
     "fhd_test_schedule": (_int, [_i64, _i64, _int]),
@@ -267,6 +273,52 @@ def fhd_compute_noalloc(kx, ky, kz, Dr, Di, x, y, z, rho_r, rho_i, mode=MODE_ACC
                                    _ptr(z), _ptr(rho_r), _ptr(rho_i), mode, _stream_ptr(stream)),
            "fhd_compute_noalloc")
     return rho_r, rho_i
+
+
+class CgWorkspace:
+    """A device buffer sized by fhd_cg_workspace_bytes, reusable across solves."""
+
+    def __init__(self, N: int, M: int, device=None):
+        import torch
+
+        dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+        self.nbytes = int(load().fhd_cg_workspace_bytes(N, M, dev.index))
+        if self.nbytes == 0:
+            raise FhdError(1, "fhd_cg_workspace_bytes")
+        self.tensor = torch.empty(self.nbytes, dtype=torch.uint8, device=dev)
+
+    @property
+    def ptr(self) -> int:
+        return self.tensor.data_ptr()
+
+
+def fhd_cg_solve(kx, ky, kz, Dr, Di, x, y, z, lam=0.0, max_iter=10, tol=0.0, rho_r=None, rho_i=None,
+                 mode=MODE_ACCURATE, workspace=None, stream=None, info=True):
+    """Conjugate gradients on (F^H F + lam I) rho = F^H D (fhd_cg_solve in fhd.h).
+
+    Returns (rho_r, rho_i, info) where info = (iterations, rs_final, stopped)
+    read back with fhd_cg_info (a synchronisation), or None when info=False.
+    """
+    import torch
+
+    lib = load()
+    _require((kx, ky, kz, Dr, Di, x, y, z, rho_r, rho_i), "fhd_cg_solve")
+    N, M = _n(x), _n(kx)
+    if rho_r is None:
+        rho_r = torch.empty(N, dtype=torch.float32, device=x.device)
+    if rho_i is None:
+        rho_i = torch.empty(N, dtype=torch.float32, device=x.device)
+    ws = workspace if workspace is not None else CgWorkspace(N, M, x.device.index)
+    st = _stream_ptr(stream)
+    _check(lib.fhd_cg_solve(M, _ptr(kx), _ptr(ky), _ptr(kz), _ptr(Dr), _ptr(Di), N, _ptr(x), _ptr(y), _ptr(z),
+                            float(lam), int(max_iter), float(tol), _ptr(rho_r), _ptr(rho_i), mode, ws.ptr,
+                            ws.nbytes, st), "fhd_cg_solve")
+    if not info:
+        return rho_r, rho_i, None
+    it, rs, stopped = ctypes.c_int(0), ctypes.c_double(0.0), ctypes.c_int(0)
+    _check(lib.fhd_cg_info(ws.ptr, st, ctypes.addressof(it), ctypes.addressof(rs), ctypes.addressof(stopped)),
+           "fhd_cg_info")
+    return rho_r, rho_i, (it.value, rs.value, stopped.value)
 
 
 def fhd_workspace_status(workspace, stream=None) -> int:

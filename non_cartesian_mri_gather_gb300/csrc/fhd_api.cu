@@ -11,32 +11,13 @@
 
 #include "../../include/fhd.h"
 #include "../../include/fhd_testing.h"
+#include "fhd_host.h"
 #include "fhd_kernels.cuh"
 
-namespace {
-
-using namespace fhd;
+namespace fhd {
+namespace host {
 
 constexpr int kVersion = 100;  // 0.1.0
-constexpr size_t kWsAlign = 256;
-constexpr size_t kHeaderBytes = 256;  // status word + reserved
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
-
-constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-// Mode word: bit 0 selects fast sin/cos, bit 1 (FHD_MODE_DIRECT) disables the
-// equal-spacing recurrence.
-bool valid_mode(fhd_mode m) { return ((int)m & ~3) == 0; }
-bool fast_mode(fhd_mode m) { return ((int)m & FHD_MODE_FAST) != 0; }
-
-struct Layout {
-    size_t packed;   // offset of packed source records
-    size_t partial;  // offset of per-CTA partial slots
-    size_t frho;     // offset of F rho (fhfrho_apply only)
-    size_t total;
-};
 
 // Resident CTAs of the gather kernel on `device` (SMs x CTAs per SM).
 cudaError_t max_ctas(int device, fhd_mode mode, int* out) {
@@ -75,11 +56,6 @@ Layout layout_for(fhd_op op, int64_t N, int64_t M, int sms) {
 
 // ---------------------------------------------------------------- validation
 typedef CUresult(CUDAAPI* PFN_range)(CUdeviceptr*, size_t*, CUdeviceptr);
-
-struct Buf {
-    const void* p;
-    size_t bytes;
-};
 
 bool overlaps(const Buf& a, const Buf& b) {
     if (a.bytes == 0 || b.bytes == 0) return false;
@@ -122,21 +98,9 @@ fhd_status check_array(const void* p, size_t bytes, size_t align, int device) {
 fhd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FHD_OK : FHD_ERR_CUDA; }
 
 // ---------------------------------------------------------------- launches
-struct GatherProblem {
-    // targets
-    int64_t n_targets;
-    const float *tx, *ty, *tz;
-    // sources
-    int64_t n_sources;
-    const float *sx, *sy, *sz, *wr, *wi;
-    float sign;  // +1: adjoint kernel; -1: forward (source coordinates negated)
-    // outputs
-    float *out_r, *out_i;
-};
-
 fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, const Layout& L, int device,
                       cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop, int64_t skip_tile,
-                      bool first_pass = true) {
+                      bool first_pass, const uint32_t* skip) {
     if (g.n_targets == 0) return FHD_OK;
     if (g.n_sources == 0) {
         cudaError_t e = first_pass ? cudaMemsetAsync(ws, 0, sizeof(uint32_t), stream) : cudaSuccess;
@@ -165,7 +129,7 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     const int pack_grid = (int)std::min<int64_t>(ceil_div(padded, 256), (int64_t)sms * 8);
     const float scale = g.sign * (fast_mode(mode) ? 6.28318530717958647692f : 1.0f);
     pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, scale, g.n_sources, padded,
-                                                packed, status, first_pass ? 1 : 0);
+                                                packed, status, first_pass ? 1 : 0, skip);
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
 
     GatherArgs a;
@@ -181,6 +145,7 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     a.wait_limit_ns = kWaitLimitNs;
     a.skip_tile = skip_tile;
     a.allow_strided = ((int)mode & FHD_MODE_DIRECT) ? 0 : 1;
+    a.skip = skip;
 
     if (ev_start && (e = cudaEventRecord(ev_start, stream)) != cudaSuccess) return FHD_ERR_CUDA;
     const size_t smem = sizeof(GatherSmem);
@@ -193,7 +158,7 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
     if (sch.ctas > 1) {
-        fixup_kernel<<<sch.ctas - 1, 256, 0, stream>>>(sch, partial, g.out_r, g.out_i);
+        fixup_kernel<<<sch.ctas - 1, 256, 0, stream>>>(sch, partial, g.out_r, g.out_i, skip);
         if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
     }
     if (ev_stop && (e = cudaEventRecord(ev_stop, stream)) != cudaSuccess) return FHD_ERR_CUDA;
@@ -278,7 +243,11 @@ fhd_status fhd_compute_impl(int64_t M, const float* kx, const float* ky, const f
     return run_gather(g, mode, (unsigned char*)workspace, L, device, stream, ev0, ev1, skip_tile);
 }
 
-}  // namespace
+}  // namespace host
+}  // namespace fhd
+
+using namespace fhd;
+using namespace fhd::host;
 
 extern "C" {
 

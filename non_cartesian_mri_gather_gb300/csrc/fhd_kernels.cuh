@@ -147,6 +147,7 @@ struct GatherArgs {
     uint64_t wait_limit_ns;          // bounded-wait time limit
     int64_t skip_tile;               // test hook: work item whose copy is never issued (-1: none)
     int allow_strided;               // 1: use the equal-spacing recurrence where it applies
+    const uint32_t* skip;            // optional device word: non-zero at launch -> do nothing
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -271,7 +272,9 @@ __device__ __forceinline__ void phasor_poly(float P, float& s, float& c) {
 __global__ void pack_sources(const float* __restrict__ ax, const float* __restrict__ ay,
                              const float* __restrict__ az, const float* __restrict__ wr,
                              const float* __restrict__ wi, float scale, int64_t n, int64_t n_padded,
-                             float4* __restrict__ out, uint32_t* status, int reset_status) {
+                             float4* __restrict__ out, uint32_t* status, int reset_status,
+                             const uint32_t* skip) {
+    if (skip != nullptr && *skip != 0u) return;
     if (reset_status && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_padded;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -492,6 +495,9 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
     extern __shared__ __align__(128) unsigned char smem_raw[];
     GatherSmem& sm = *reinterpret_cast<GatherSmem*>(smem_raw);
 
+    // A set skip word (written by an earlier kernel on the stream, never while
+    // this one runs) makes every thread return before any barrier or wait.
+    if (args.skip != nullptr && *args.skip != 0u) return;
     const Schedule& sch = args.sch;
     const int c = blockIdx.x;
     const int64_t w_begin = sch.start(c);
@@ -647,7 +653,8 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
 // block b means b was split; the lowest such boundary sums b's partial slots
 // over the contributing CTAs c-1 .. c_hi in increasing order.
 __global__ void fixup_kernel(const Schedule sch, const float* __restrict__ partial, float* __restrict__ out_r,
-                             float* __restrict__ out_i) {
+                             float* __restrict__ out_i, const uint32_t* skip) {
+    if (skip != nullptr && *skip != 0u) return;
     const int64_t c = (int64_t)blockIdx.x + 1;
     const int64_t b = sch.fixup_block(c);
     if (b < 0) return;
