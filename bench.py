@@ -99,6 +99,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--ladder", action="store_true",
+                    help="time the case study's optimisation ladder (include/fhd_ladder.h) next to the library "
+                         "on workloads 1 and 2 instead of the benchmark line (one JSON line per variant)")
     return ap.parse_args()
 
 
@@ -466,8 +469,52 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_ladder(args):
+    """One JSON line per (workload, variant): the ladder steps L0-L5, the scatter
+    form (workload 1 only: its atomics serialise on every voxel) and the
+    library's accurate and fast paths, timed with CUDA events after warm-up."""
+    import torch
+
+    import non_cartesian_mri_gather_gb300 as fhd
+
+    fhd.load()
+    for wl in (1, 2):
+        p = load_workload(wl)
+        d = {k: torch.from_numpy(getattr(p, k)).cuda() for k in ("kx", "ky", "kz", "Dr", "Di", "x", "y", "z")}
+        args_t = (d["kx"], d["ky"], d["kz"], d["Dr"], d["Di"], d["x"], d["y"], d["z"])
+        runs = [(v, lambda v=v: fhd.fhd_compute_variant(v, *args_t)) for v in fhd.VARIANTS
+                if not (v == "scatter" and wl != 1)]
+        ws = fhd.Workspace(fhd.OP_FHD, p.N, p.M)
+        for name, mode in (("library accurate", fhd.MODE_ACCURATE), ("library fast", fhd.MODE_FAST)):
+            runs.append((name, lambda mode=mode: fhd.fhd_compute(*args_t, mode=mode, workspace=ws)))
+        ref = None
+        for name, fn in runs:
+            for _ in range(max(1, args.warmup)):
+                out = fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(1, args.steps)
+            a.record()
+            for _ in range(reps):
+                out = fn()
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / reps
+            val = torch.complex(out[0].double(), out[1].double()).cpu().numpy()
+            if ref is None:
+                ref = val
+            rel = float(np.linalg.norm(val - ref) / np.linalg.norm(ref))
+            pairs = p.N * p.M
+            print(json.dumps({"ladder": name, "workload": WORKLOAD_NAMES[wl], "ms": ms, "pairs_per_s": pairs / (ms * 1e-3),
+                              "gflops_13": FLOP_PER_PAIR * pairs / (ms * 1e-3) / 1e9,
+                              "rel_l2_vs_naive": rel}), flush=True)
+
+
 def main():
     args = parse()
+    if args.ladder:
+        run_ladder(args)
+        return
     world, rank, local = dist_init()
     try:
         if args.impl == "reference":

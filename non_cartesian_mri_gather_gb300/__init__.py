@@ -44,6 +44,8 @@ __all__ = [
     "fhd_version",
     "fhd_compute_noalloc",
     "fhd_cg_solve",
+    "fhd_compute_variant",
+    "VARIANTS",
     "CgWorkspace",
     "Workspace",
 ]
@@ -91,6 +93,8 @@ SIGNATURES = {
     "fhd_cg_solve": (_int, [_i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, ctypes.c_float, _int,
                             ctypes.c_double, _vp, _vp, _int, _vp, _sz, _vp]),
     "fhd_cg_info": (_int, [_vp, _vp, _vp, _vp, _vp]),
+    "fhd_variant_workspace_bytes": (_sz, [_int, _i64, _i64]),
+    "fhd_compute_variant": (_int, [_int, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fhd_test_compute_skip_tile": (_int, [_i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp,
                                           _sz, _vp, _i64]),
     "fhd_test_schedule": (_int, [_i64, _i64, _int]),
@@ -319,6 +323,35 @@ def fhd_cg_solve(kx, ky, kz, Dr, Di, x, y, z, lam=0.0, max_iter=10, tol=0.0, rho
     _check(lib.fhd_cg_info(ws.ptr, st, ctypes.addressof(it), ctypes.addressof(rs), ctypes.addressof(stopped)),
            "fhd_cg_info")
     return rho_r, rho_i, (it.value, rs.value, stopped.value)
+
+
+# Comparison kernels of include/fhd_ladder.h: the case study's optimisation
+# ladder (L0-L5) and the scatter form.
+VARIANTS = {"naive": 0, "fission": 1, "private": 2, "constant": 3, "intrinsics": 4, "unroll": 5, "scatter": 6}
+
+
+def fhd_compute_variant(variant, kx, ky, kz, Dr, Di, x, y, z, rho_r=None, rho_i=None, workspace=None,
+                        stream=None):
+    """rho = F^H D with one step of the ladder (`variant`: a VARIANTS key or code)."""
+    import torch
+
+    lib = load()
+    v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    _require((kx, ky, kz, Dr, Di, x, y, z, rho_r, rho_i), "fhd_compute_variant")
+    N, M = _n(x), _n(kx)
+    if rho_r is None:
+        rho_r = torch.empty(N, dtype=torch.float32, device=x.device)
+    if rho_i is None:
+        rho_i = torch.empty(N, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        nb = int(lib.fhd_variant_workspace_bytes(v, N, M))
+        if nb == 0:
+            raise FhdError(1, "fhd_variant_workspace_bytes")
+        workspace = torch.empty(nb, dtype=torch.uint8, device=x.device)
+    _check(lib.fhd_compute_variant(v, M, _ptr(kx), _ptr(ky), _ptr(kz), _ptr(Dr), _ptr(Di), N, _ptr(x), _ptr(y),
+                                   _ptr(z), _ptr(rho_r), _ptr(rho_i), workspace.data_ptr(), workspace.numel(),
+                                   _stream_ptr(stream)), "fhd_compute_variant")
+    return rho_r, rho_i
 
 
 def fhd_workspace_status(workspace, stream=None) -> int:
