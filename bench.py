@@ -463,7 +463,7 @@ def run_ours(args, world, rank, local):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,  # pack, describe, gather, fix-up per step
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -230,7 +230,7 @@ FHD_API fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *t
  */
 #define FHD_NOALLOC_MAX_SAMPLES 131072
 #define FHD_NOALLOC_MAX_CTAS 160
-#define FHD_NOALLOC_SCRATCH_BYTES (512 + (size_t)FHD_NOALLOC_MAX_SAMPLES * 32 + \
+#define FHD_NOALLOC_SCRATCH_BYTES (768 + (size_t)FHD_NOALLOC_MAX_SAMPLES * 33 + \
                                    (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * 6144 * 4)
 FHD_API fhd_status fhd_compute_noalloc(int64_t M, const float *kx, const float *ky, const float *kz,
                                const float *Dr, const float *Di,

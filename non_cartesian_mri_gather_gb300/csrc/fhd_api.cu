@@ -46,6 +46,8 @@ Layout layout_for(fhd_op op, int64_t N, int64_t M, int sms) {
     size_t off = kHeaderBytes;
     L.packed = off;
     off = align_up(off + (size_t)padded * kRecordBytes, kWsAlign);
+    L.desc = off;
+    off = align_up(off + (size_t)(padded / kSegment) * 16, kWsAlign);
     L.partial = off;
     off = align_up(off + (size_t)(2 * ctas) * 2 * kTargetsPerBlock * sizeof(float), kWsAlign);
     L.frho = off;
@@ -131,6 +133,11 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, scale, g.n_sources, padded,
                                                 packed, status, first_pass ? 1 : 0, skip);
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
+    float4* desc = reinterpret_cast<float4*>(ws + L.desc);
+    const int64_t n_segments = padded / kSegment;
+    const int desc_grid = (int)std::min<int64_t>(ceil_div(n_segments, 256), (int64_t)sms * 8);
+    describe_segments<<<desc_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, scale, g.n_sources, n_segments, desc, skip);
+    if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
 
     GatherArgs a;
     a.sch = sch;
@@ -138,6 +145,7 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     a.ty = g.ty;
     a.tz = g.tz;
     a.packed = packed;
+    a.desc = desc;
     a.out_r = g.out_r;
     a.out_i = g.out_i;
     a.partial = partial;
@@ -379,6 +387,7 @@ namespace {
 // targets per block); builds with other shape constants size the array for
 // their own layout.
 constexpr size_t kNoAllocLayoutBytes = kHeaderBytes + (size_t)FHD_NOALLOC_MAX_SAMPLES * kRecordBytes + kWsAlign +
+                                       (size_t)FHD_NOALLOC_MAX_SAMPLES / kSegment * 16 + kWsAlign +
                                        (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * kTargetsPerBlock * sizeof(float);
 constexpr size_t kNoAllocScratchBytes =
     FHD_NOALLOC_SCRATCH_BYTES > kNoAllocLayoutBytes ? FHD_NOALLOC_SCRATCH_BYTES : kNoAllocLayoutBytes;

@@ -79,6 +79,13 @@ constexpr int kTile = FHD_TILE;          // sources per staged tile
 constexpr int kStages = FHD_STAGES;      // shared-memory ring depth
 constexpr int kRecordBytes = 32;         // one packed source
 constexpr int kTileBytes = kTile * kRecordBytes;
+// Source segments: kSegment consecutive packed sources whose coordinates are
+// exactly equally spaced take the source-side recurrence; one 16-byte
+// descriptor {step.x, step.y, step.z, flag} per segment, kDescBytes per tile.
+constexpr int kSegment = 16;
+constexpr int kSegmentsPerTile = kTile / kSegment;
+constexpr int kDescBytes = kSegmentsPerTile * 16;
+static_assert(kTile % kSegment == 0, "tiles hold whole segments");
 constexpr int kCtaThreads = kThreads + 32;  // + one producer warp
 constexpr int kMinCtasPerSm = FHD_MIN_CTAS_PER_SM;
 constexpr int kUnroll = FHD_UNROLL;      // sources per unrolled inner-loop step
@@ -140,6 +147,7 @@ struct GatherArgs {
     const float* __restrict__ ty;
     const float* __restrict__ tz;
     const float4* __restrict__ packed;  // n_tiles * kTile records of 2 float4
+    const float4* __restrict__ desc;    // n_tiles * kSegmentsPerTile segment descriptors
     float* __restrict__ out_r;
     float* __restrict__ out_i;
     float* __restrict__ partial;    // [2*ctas slots][2][kTargetsPerBlock]
@@ -290,9 +298,40 @@ __global__ void pack_sources(const float* __restrict__ ax, const float* __restri
     }
 }
 
+// Segment descriptors: one thread per kSegment sources.  A segment is flagged
+// when its real sources (index < n) have coordinates a_s = a_0 + (s - s0) * D
+// exactly (checked in double on the caller's unscaled coordinates, where these
+// products and sums are exact); the descriptor holds the scaled step
+// scale * D rounded once to float32.  The packed coordinates are
+// fl(scale * a_s), so A_0 + s * fl(scale * D) differs from them only by
+// rounding (fast mode's scale 2 pi breaks exact spacing of the packed values
+// themselves).  Sources at index >= n are zero-weight padding.
+__global__ void describe_segments(const float* __restrict__ ax, const float* __restrict__ ay,
+                                  const float* __restrict__ az, float scale, int64_t n, int64_t n_segments,
+                                  float4* __restrict__ desc, const uint32_t* skip) {
+    if (skip != nullptr && *skip != 0u) return;
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < n_segments;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t s0 = g * kSegment;
+        const int64_t real = n - s0 < kSegment ? (n - s0 > 0 ? n - s0 : 0) : kSegment;
+        float4 out = make_float4(0.f, 0.f, 0.f, 1.f);
+        if (real >= 2) {
+            const double x0 = ax[s0], y0 = ay[s0], z0 = az[s0];
+            const double dx = (double)ax[s0 + 1] - x0, dy = (double)ay[s0 + 1] - y0, dz = (double)az[s0 + 1] - z0;
+            bool ok = true;
+            for (int64_t s = 2; s < real && ok; ++s)
+                ok = (double)ax[s0 + s] == x0 + (double)s * dx && (double)ay[s0 + s] == y0 + (double)s * dy &&
+                     (double)az[s0 + s] == z0 + (double)s * dz;
+            out = make_float4((float)(scale * dx), (float)(scale * dy), (float)(scale * dz), ok ? 1.f : 0.f);
+        }
+        desc[g] = out;
+    }
+}
+
 // ---------------------------------------------------------------- gather
 struct __align__(16) GatherSmem {
     float4 ring[kStages][kTile * 2];
+    float4 desc[kStages][kSegmentsPerTile];
     // Running sums of the current segment, one private column per consumer
     // thread (rows: kV real parts, then kV imaginary parts).  They are touched
     // once per tile, so keeping them here instead of in registers frees
@@ -487,6 +526,93 @@ __device__ __forceinline__ bool equally_spaced(const float (&c)[kV], int n, floa
     return ok;
 }
 
+// Source-side recurrence, for tiles whose every segment of kSegment sources
+// is equally spaced (a row of an image grid when the voxels are the sources,
+// as in the forward sum F rho).  For target b and segment sources
+// A_s = A_0 + s d: exp(i A_s.b) = e_0 u^s with e_0 = exp(i A_0.b) and
+// u = exp(i d.b).  Per (target, segment) two phasors; per source the real and
+// imaginary parts of e_s step by the three-term recurrence
+// e_{s+1} = 2 cos(d.b) e_s - e_{s-1} (two FFMA; error growth at most
+// eps * s^2 / 2 over the kSegment sources) and the complex multiply-accumulate
+// adds w_s e_s.  Targets go in groups of kDirectGroup; each group's tile sums
+// are folded straight into the thread's running sums.
+template <int MODE>
+__device__ __forceinline__ void accumulate_tile_src_strided(const float4* __restrict__ rec,
+                                                            const float4* __restrict__ desc,
+                                                            const float (*coord)[kThreads], float (*run)[kThreads],
+                                                            int tid) {
+#pragma unroll 1
+    for (int g = 0; g < kV; g += kDirectGroup) {
+        float bx[kDirectGroup], by[kDirectGroup], bz[kDirectGroup];
+        float ar[kDirectGroup], ai[kDirectGroup];
+#pragma unroll
+        for (int v = 0; v < kDirectGroup; ++v) {
+            bx[v] = coord[g + v][tid];
+            by[v] = coord[kV + g + v][tid];
+            bz[v] = coord[2 * kV + g + v][tid];
+            ar[v] = 0.f;
+            ai[v] = 0.f;
+        }
+#pragma unroll 1
+        for (int j = 0; j < kSegmentsPerTile; ++j) {
+            const float4 b0 = rec[2 * j * kSegment];      // A_0.x A_0.x A_0.y A_0.y
+            const float4 b1 = rec[2 * j * kSegment + 1];  // A_0.z A_0.z w.re w.im
+            const float4 d = desc[j];
+            float er[kDirectGroup], ei[kDirectGroup], pr[kDirectGroup], pi[kDirectGroup], c2[kDirectGroup];
+#pragma unroll
+            for (int v = 0; v < kDirectGroup; ++v) {
+                const float p0 = fmaf(b1.x, bz[v], fmaf(b0.z, by[v], b0.x * bx[v]));
+                const float pd = fmaf(d.z, bz[v], fmaf(d.y, by[v], d.x * bx[v]));
+                float s0, c0, su, cu;
+                if constexpr (MODE == kAccurate) {
+                    phasor_accurate(p0, s0, c0);
+                    phasor_accurate(pd, su, cu);
+                } else {
+                    phasor_mufu(p0, s0, c0);
+                    phasor_mufu(pd, su, cu);
+                }
+                pr[v] = c0;  // e_0
+                pi[v] = s0;
+                er[v] = fmaf(c0, cu, -s0 * su);  // e_1 = e_0 u
+                ei[v] = fmaf(c0, su, s0 * cu);
+                c2[v] = cu + cu;
+            }
+            // source 0 uses e_0, sources 1.. use e_1, e_2, ...
+#pragma unroll
+            for (int v = 0; v < kDirectGroup; ++v) {
+                ar[v] = fmaf(b1.z, pr[v], ar[v]);
+                ar[v] = fmaf(-b1.w, pi[v], ar[v]);
+                ai[v] = fmaf(b1.z, pi[v], ai[v]);
+                ai[v] = fmaf(b1.w, pr[v], ai[v]);
+            }
+#pragma unroll
+            for (int s = 1; s < kSegment; ++s) {
+                const float4 w = rec[2 * (j * kSegment + s) + 1];  // w.re, w.im in .z, .w
+#pragma unroll
+                for (int v = 0; v < kDirectGroup; ++v) {
+                    ar[v] = fmaf(w.z, er[v], ar[v]);
+                    ar[v] = fmaf(-w.w, ei[v], ar[v]);
+                    ai[v] = fmaf(w.z, ei[v], ai[v]);
+                    ai[v] = fmaf(w.w, er[v], ai[v]);
+                    if (s + 1 < kSegment) {
+                        const float nr = fmaf(c2[v], er[v], -pr[v]);
+                        const float ni = fmaf(c2[v], ei[v], -pi[v]);
+                        pr[v] = er[v];
+                        pi[v] = ei[v];
+                        er[v] = nr;
+                        ei[v] = ni;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < kDirectGroup; ++v) {
+            run[g + v][tid] += ar[v];
+            run[kV + g + v][tid] += ai[v];
+        }
+    }
+}
+
 // MODE: kAccurate or kFast.  NPOLY (fast mode only): how many of the kV
 // register slots evaluate sin/cos with the FMA-pipe polynomial instead of the
 // MUFU pipe; it sets the split between the two pipes.
@@ -529,8 +655,9 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
             }
             if (w == args.skip_tile) continue;  // test hook: this copy never arrives
             const int64_t j = w % sch.n_tiles;
-            mbar_arrive_expect_tx(&sm.full[st], kTileBytes);
+            mbar_arrive_expect_tx(&sm.full[st], kTileBytes + kDescBytes);
             bulk_copy_g2s(&sm.ring[st][0], args.packed + j * (kTile * 2), kTileBytes, &sm.full[st]);
+            bulk_copy_g2s(&sm.desc[st][0], args.desc + j * kSegmentsPerTile, kDescBytes, &sm.full[st]);
         }
         // Drain: the last copy issued into each stage must have landed before
         // this CTA's shared memory can be released.
@@ -610,12 +737,19 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
                 }
             }
         } else {
-            float tr[kV], ti[kV];
-            accumulate_tile<MODE, NPOLY>(rec, sm.coord, tid, tr, ti);
+            bool src_strided = args.allow_strided != 0;
 #pragma unroll
-            for (int v = 0; v < kV; ++v) {
-                sm.run[v][tid] += tr[v];
-                sm.run[kV + v][tid] += ti[v];
+            for (int q = 0; q < kSegmentsPerTile; ++q) src_strided = src_strided && sm.desc[st][q].w != 0.f;
+            if (src_strided) {
+                accumulate_tile_src_strided<MODE>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
+            } else {
+                float tr[kV], ti[kV];
+                accumulate_tile<MODE, NPOLY>(rec, sm.coord, tid, tr, ti);
+#pragma unroll
+                for (int v = 0; v < kV; ++v) {
+                    sm.run[v][tid] += tr[v];
+                    sm.run[kV + v][tid] += ti[v];
+                }
             }
         }
         __syncwarp();

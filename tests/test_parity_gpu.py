@@ -204,6 +204,74 @@ def test_fwd_radial_spokes(mode):
     check(gpu_fwd(p, mode), ref, mode, "F rho radial")
 
 
+# ------------------------------------------------------------ source-side recurrence
+
+def _spokes(n_spokes, seed):
+    """Samples along radial spokes whose directions are multiples of 2^-12:
+    every sample r*d is exact in float32, so the samples of a spoke are
+    exactly equally spaced."""
+    rng = np.random.default_rng(seed)
+    d = rng.standard_normal((n_spokes, 3))
+    d /= np.linalg.norm(d, axis=1, keepdims=True)
+    d = np.round(d * 4096) / 4096
+    r = np.arange(256) - 128.0
+    return (d[:, None, :] * r[None, :, None]).reshape(-1, 3).astype(np.float32)
+
+
+@pytest.mark.parametrize("side", [32, 24])
+@pytest.mark.parametrize("mode", ALL_MODES)
+def test_fwd_grid_voxel_sources(side, mode):
+    """F rho with the voxels of a side^3 grid as sources: rows of 32 split into
+    equally spaced 16-source segments (source recurrence); rows of 24 make
+    segments straddle rows, so those tiles are evaluated pair by pair."""
+    from inputs import grid_coords
+
+    x, y, z = grid_coords(side, side, side)
+    p = random_problem(x.size, 1500, kmax=side / 2, seed=side, op="fwd")
+    p.x, p.y, p.z = x, y, z
+    ref = oracle.forward(p.x, p.y, p.z, p.rho_r + 1j * p.rho_i, p.kx, p.ky, p.kz)
+    check(gpu_fwd(p, mode), ref, mode, f"F rho, {side}^3 voxel sources")
+
+
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_fwd_perturbed_voxel_sources(mode):
+    from inputs import grid_coords
+
+    x, y, z = grid_coords(32, 32, 32)
+    x = x.copy()
+    x[5000] = np.nextafter(x[5000], np.float32(1.0))  # breaks one segment: its tile goes pair by pair
+    p = random_problem(x.size, 1000, kmax=16.0, seed=8, op="fwd")
+    p.x, p.y, p.z = x, y, z
+    ref = oracle.forward(p.x, p.y, p.z, p.rho_r + 1j * p.rho_i, p.kx, p.ky, p.kz)
+    check(gpu_fwd(p, mode), ref, mode, "F rho, perturbed voxel sources")
+
+
+def test_source_recurrence_differs_from_direct_but_both_match():
+    from inputs import grid_coords
+
+    x, y, z = grid_coords(32, 32, 32)
+    p = random_problem(x.size, 2000, kmax=16.0, seed=9, op="fwd")
+    p.x, p.y, p.z = x, y, z
+    ref = oracle.forward(p.x, p.y, p.z, p.rho_r + 1j * p.rho_i, p.kx, p.ky, p.kz)
+    for fast in (0, 1):
+        a = gpu_fwd(p, fast)
+        b = gpu_fwd(p, fast | 2)
+        check(a, ref, fast, "source recurrence")
+        check(b, ref, fast | 2, "direct")
+        assert not np.array_equal(a, b), "the source recurrence did not run"
+
+
+@pytest.mark.parametrize("mode", ALL_MODES)
+def test_fhd_spoke_sources_random_voxels(mode):
+    """F^H D with exactly spaced spoke samples as sources and scattered voxels
+    as targets: the source recurrence, not the target one."""
+    k = _spokes(11, 10)
+    p = random_problem(5000, k.shape[0], kmax=1.0, seed=11)
+    p.kx, p.ky, p.kz = (np.ascontiguousarray(k[:, i]) for i in range(3))
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    check(gpu_fhd(p, mode), ref, mode, "F^H D spoke sources")
+
+
 # ------------------------------------------------------------ edge cases
 
 def test_empty_and_zero_sources():
