@@ -67,6 +67,12 @@ def per_pair_counts(path: str):
     if path == "direct":
         # k.x (1 FMUL + 2 FFMA) + complex MAC (4 FFMA); sin, cos
         return 7.0, 2.0, 9.0
+    if path == "source":
+        # source-side recurrence, segments of S = 16 sources: per pair a
+        # three-term step (2) and the complex MAC (4); per (target, segment)
+        # two phases (6), e_1 = e_0 u (4), 2 cos (1) and 4 MUFU
+        S = 16.0
+        return 6.0 + 11.0 / S, 4.0 / S, 6.0 + 15.0 / S
     # recurrence, V targets per thread.  Per (thread, sample): the two phases
     # as 3 packed instructions (6 lane operations), g_0 = D exp(i theta_0) (4),
     # g_1 = g_0 u (4), 2 cos(theta_d) (1), 4 MUFU.  Per target: one packed add
@@ -202,6 +208,13 @@ def load_workload(i: int):
 
 
 def peak_pairs_per_s(sms: int, mhz: float, path: str = "direct") -> float:
+    if path == "fhf":
+        # F^H F rho: half the pairs in the forward gather (source recurrence),
+        # half in the adjoint gather (target recurrence); the bound of the
+        # whole is the pair-weighted harmonic mean of the two.
+        a = peak_pairs_per_s(sms, mhz, "source")
+        b = peak_pairs_per_s(sms, mhz, "recurrence")
+        return 2.0 / (1.0 / a + 1.0 / b)
     n_fma, n_mufu, n_issue = per_pair_counts(path)
     per_clk = min(FMA_LANES_PER_SM / n_fma, MUFU_LANES_PER_SM / n_mufu, ISSUE_PER_SM / n_issue)
     return sms * per_clk * mhz * 1e6
@@ -320,21 +333,29 @@ def run_ours(args, world, rank, local):
     # voxels are exactly equally spaced, so the recurrence runs unless disabled.
     path = "direct" if args.mode.endswith("direct") else "recurrence"
     p = load_workload(args.workload)
-    if p.op == "fhf":
-        raise SystemExit("bench.py times the F^H D workloads 1-4; workload 5 is covered by the tests")
-    names = ("kx", "ky", "kz", "Dr", "Di", "x", "y", "z")
+    fhf = p.op == "fhf"
+    if fhf:  # F^H F rho: the forward gather (voxel sources) then the adjoint gather
+        path = "direct" if args.mode.endswith("direct") else "fhf"
+    names = ("x", "y", "z", "rho_r", "rho_i", "kx", "ky", "kz") if fhf else ("kx", "ky", "kz", "Dr", "Di", "x", "y", "z")
     host = {k: torch.from_numpy(getattr(p, k)) for k in names}
     d = {k: v.to(dev) for k, v in host.items()}
     rho_r = torch.empty(p.N, dtype=torch.float32, device=dev)
     rho_i = torch.empty(p.N, dtype=torch.float32, device=dev)
-    ws = fhd.Workspace(fhd.OP_FHD, p.N, p.M, local)
+    ws = fhd.Workspace(fhd.OP_FHF if fhf else fhd.OP_FHD, p.N, p.M, local)
     stream = torch.cuda.current_stream(dev)
     shape = fhd.fhd_launch_shape(local, mode)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     input_bytes = sum(v.numel() * 4 for v in d.values())
 
     def step(e0=None, e1=None):
-        if e0 is None:
+        if fhf:
+            if e0 is not None:
+                e0.record(stream)
+            fhd.fhfrho_apply(d["x"], d["y"], d["z"], d["rho_r"], d["rho_i"], d["kx"], d["ky"], d["kz"], rho_r, rho_i,
+                             mode=mode, workspace=ws)
+            if e1 is not None:
+                e1.record(stream)
+        elif e0 is None:
             fhd.fhd_compute(d["kx"], d["ky"], d["kz"], d["Dr"], d["Di"], d["x"], d["y"], d["z"], rho_r, rho_i,
                             mode=mode, workspace=ws)
         else:
@@ -369,7 +390,7 @@ def run_ours(args, world, rank, local):
     ms_local = start.elapsed_time(stop) / args.steps
     ms = max_over_ranks(ms_local, world)
     gather_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    pairs = p.N * p.M
+    pairs = p.pairs
     value = world * pairs / (ms * 1e-3)
 
     # ---- end to end through the public API with pinned host buffers
@@ -409,7 +430,7 @@ def run_ours(args, world, rank, local):
     max_mhz = float(peaks.get("sm_max_mhz") or clk.get("sm_max_mhz") or 2070.0)
     peak = peak_pairs_per_s(sms, max_mhz, path)
     achieved = pairs / (gather_ms * 1e-3)
-    n_fma, n_mufu, n_issue = per_pair_counts(path)
+    n_fma, n_mufu, n_issue = per_pair_counts("recurrence" if path == "fhf" else path)
     roof = {
         "bound": "alu",
         "achieved": FLOP_PER_PAIR * achieved / 1e12,
@@ -418,12 +439,14 @@ def run_ours(args, world, rank, local):
         "frac": achieved / peak,
         "traffic": profiled_traffic(args.workload, args.mode),
         "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
-        "kernel": "gather_kernel",
+        "kernel": "gather_kernel" if not fhf else "gather_kernel x2 (whole fhfrho_apply call)",
         "kernel_ms": gather_ms,
         "path": path,
         "peak_basis": (f"{sms} SMs x {max_mhz:.0f} MHz x min({FMA_LANES_PER_SM}/{n_fma:g}, "
                        f"{MUFU_LANES_PER_SM}/{n_mufu:g}, {ISSUE_PER_SM}/{n_issue:g}) pairs/clk x "
-                       f"{FLOP_PER_PAIR} flop/pair ({path} path)"),
+                       f"{FLOP_PER_PAIR} flop/pair ({path} path)") if path != "fhf" else (
+            f"{sms} SMs x {max_mhz:.0f} MHz, pair-weighted harmonic mean of the forward gather's "
+            f"source-recurrence bound and the adjoint gather's target-recurrence bound x {FLOP_PER_PAIR} flop/pair"),
         "direct_path_peak": FLOP_PER_PAIR * peak_pairs_per_s(sms, max_mhz, "direct") / 1e12,
     }
     if clk.get("sm_mhz"):
@@ -435,7 +458,7 @@ def run_ours(args, world, rank, local):
         cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
 
     line = {
-        "metric": "F^H D voxel-sample pairs/s",
+        "metric": "F^H F rho voxel-sample pairs/s (both passes)" if fhf else "F^H D voxel-sample pairs/s",
         "value": value,
         "unit": "pairs/s",
         "gflops": FLOP_PER_PAIR * value / 1e9,
