@@ -21,7 +21,7 @@ roofline   the gather kernel against its plain-ALU bound
            are the algorithm's FP32 lane operations, MUFU operations and
            instructions per pair.  Pair by pair (direct): 7, 2, 9 (k.x and the
            complex MAC; sin, cos).  Equal-spacing recurrence on the benchmark's
-           grid voxels, V = 16 targets per thread, packed f32x2 arithmetic:
+           grid voxels, V = 32 targets per thread, packed f32x2 arithmetic:
            per target one packed add and (from the third target on) one packed
            three-term step, plus per (thread, sample) the two phases (3 packed
            instructions), D*exp(i theta_0) (4), its first step (4),
@@ -57,7 +57,7 @@ FMA_LANES_PER_SM = 128   # fp32 FMA-pipe results per SM per clock
 MUFU_LANES_PER_SM = 16   # sin/cos results per SM per clock (measured on GB300)
 ISSUE_PER_SM = 128       # 4 schedulers x 1 warp instruction (32 lanes) per clock
 L2_BYTES = 129 * 1024 * 1024
-TARGETS_PER_THREAD = 16
+TARGETS_PER_THREAD = 32
 
 
 def per_pair_counts(path: str):

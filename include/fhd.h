@@ -51,13 +51,16 @@
  *            hardware sin/cos approximations, partly replaced by an FMA-pipe
  *            polynomial (relative L2 error below 1e-3).  Either may be OR-ed
  *            with FHD_MODE_DIRECT, see below.
- * Spacing    where a thread's 16 consecutive targets (voxels for F^H D,
+ * Spacing    where a thread's 32 consecutive targets (voxels for F^H D,
  *            samples for F rho) are exactly equally spaced, as the voxels of a
  *            regular image grid are, the kernel evaluates two phasors per
  *            (thread, source) and reaches the other targets by the recurrence
  *            exp(i 2 pi k.(x0 + v d)) = exp(i 2 pi k.x0) exp(i 2 pi k.d)^v,
  *            an exact identity evaluated in fp32 (same tolerances).  Other
- *            targets are evaluated pair by pair.  FHD_MODE_DIRECT forces the
+ *            targets are evaluated pair by pair.  Likewise, where runs of
+ *            16 consecutive sources are exactly equally spaced (the voxels of
+ *            a grid row as sources of F rho), each target evaluates two
+ *            phasors per run and steps the rest by the same recurrence.  FHD_MODE_DIRECT forces the
  *            pair-by-pair evaluation everywhere.
  * Results are bit-identical from run to run on the same device: the sample
  * dimension is split among CTAs in a fixed way and the partial sums are
@@ -216,7 +219,7 @@ FHD_API fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *t
  * problems return FHD_ERR_TOO_LARGE before anything is launched; N is not
  * limited.
  *
- * Memory: every GPU that loads the library holds the array (about 19 MiB)
+ * Memory: every GPU that loads the library holds the array (about 25 MiB)
  * until the process exits.  The first call on a device, with that device
  * current, looks up the array's device address (cudaGetSymbolAddress) and
  * caches it; make that first call before any stream capture begins.
@@ -231,7 +234,7 @@ FHD_API fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *t
 #define FHD_NOALLOC_MAX_SAMPLES 131072
 #define FHD_NOALLOC_MAX_CTAS 160
 #define FHD_NOALLOC_SCRATCH_BYTES (768 + (size_t)FHD_NOALLOC_MAX_SAMPLES * 33 + \
-                                   (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * 6144 * 4)
+                                   (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * 8192 * 4)
 FHD_API fhd_status fhd_compute_noalloc(int64_t M, const float *kx, const float *ky, const float *kz,
                                const float *Dr, const float *Di,
                                int64_t N, const float *x, const float *y, const float *z,

@@ -383,7 +383,7 @@ int fhd_version(void) { return kVersion; }
 // partial slot the fix-up reads is written by its CTA first).
 namespace {
 
-// FHD_NOALLOC_SCRATCH_BYTES is the size for the default launch shape (6144
+// FHD_NOALLOC_SCRATCH_BYTES is the size for the default launch shape (8192
 // targets per block); builds with other shape constants size the array for
 // their own layout.
 constexpr size_t kNoAllocLayoutBytes = kHeaderBytes + (size_t)FHD_NOALLOC_MAX_SAMPLES * kRecordBytes + kWsAlign +

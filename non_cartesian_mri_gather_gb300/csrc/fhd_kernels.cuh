@@ -50,16 +50,16 @@ namespace fhd {
 // ---------------------------------------------------------------- shape
 // Compile-time launch shape (overridable with -D for tuning builds).
 #ifndef FHD_THREADS
-#define FHD_THREADS 384
+#define FHD_THREADS 256
 #endif
 #ifndef FHD_V
-#define FHD_V 16
+#define FHD_V 32
 #endif
 #ifndef FHD_TILE
-#define FHD_TILE 128
+#define FHD_TILE 256
 #endif
 #ifndef FHD_STAGES
-#define FHD_STAGES 4
+#define FHD_STAGES 6
 #endif
 #ifndef FHD_MIN_CTAS_PER_SM
 #define FHD_MIN_CTAS_PER_SM 1
@@ -99,7 +99,10 @@ constexpr uint32_t kStatusDrainTimeout = 4u;
 enum Mode : int { kAccurate = 0, kFast = 1 };
 // The pair-by-pair path walks a thread's kV targets in groups of kDirectGroup
 // (coordinates of one group in registers at a time).
-constexpr int kDirectGroup = kV < 8 ? kV : 8;
+#ifndef FHD_DIRECT_GROUP
+#define FHD_DIRECT_GROUP 8
+#endif
+constexpr int kDirectGroup = kV < FHD_DIRECT_GROUP ? kV : FHD_DIRECT_GROUP;
 static_assert(kV % kDirectGroup == 0, "kV must be a multiple of the direct-path group");
 constexpr int kFastPolySlots = FHD_FAST_POLY_SLOTS;  // of kDirectGroup: share of sin/cos on the FMA pipe
 static_assert(kFastPolySlots >= 0 && kFastPolySlots <= kDirectGroup, "bad polynomial split");

@@ -1,7 +1,7 @@
 """GPU parity: the CUDA library against the fp64 oracle, element by element.
 
 Small problems are compared on every output; they span several target blocks
-(2048 targets) and source tiles (128 sources) with ragged tails.  The five
+(8192 targets) and source tiles (256 sources) with ragged tails.  The five
 benchmark workloads run at full size in the launch configuration the
 benchmark uses; workloads 1-2 are compared on every voxel, workloads 3-4 on a
 fixed spread of sampled voxels (a gather output depends only on its own voxel,
@@ -154,14 +154,29 @@ def test_workload5(mode):
 
 # ------------------------------------------------------------ equal-spacing recurrence
 
-@pytest.mark.parametrize("N,M", [(4096, 1000), (5000, 777), (70000, 300)])
+@pytest.mark.parametrize("N,M", [(8197, 1000), (30000, 777), (65536, 300)])
 @pytest.mark.parametrize("mode", ALL_MODES)
 def test_fhd_3d_grid_ragged(N, M, mode):
-    """First N voxels of a 3D grid: rows of equally spaced voxels (recurrence),
-    a ragged last row and a ragged last block."""
-    p = random_problem(N, M, kmax=32.0, seed=N + M, coords="grid")
+    """First N voxels of a 64 x 64 x 16 grid: rows of 64 equally spaced voxels
+    (the recurrence runs on 32 per thread), a ragged last row and a ragged last
+    block of 8192 targets."""
+    from inputs import grid_coords
+
+    gx, gy, gz = grid_coords(64, 64, 16)
+    p = random_problem(N, M, kmax=32.0, seed=N + M)
+    p.x, p.y, p.z = gx[:N].copy(), gy[:N].copy(), gz[:N].copy()
     ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
     check(gpu_fhd(p, mode), ref, mode, f"F^H D grid N={N} M={M}")
+
+
+@pytest.mark.parametrize("N,M", [(4096, 1000), (5000, 777)])
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_fhd_small_grid_rows(N, M, mode):
+    """16- and 18-wide rows: shorter than a thread's 32 targets, so these warps
+    evaluate pair by pair."""
+    p = random_problem(N, M, kmax=32.0, seed=N + M, coords="grid")
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    check(gpu_fhd(p, mode), ref, mode, f"F^H D small grid N={N} M={M}")
 
 
 @pytest.mark.parametrize("mode", [ACC, FAST])
