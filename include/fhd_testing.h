@@ -32,6 +32,30 @@ FHD_API fhd_status fhd_test_compute_skip_tile(int64_t M, const float *kx, const 
                                       int64_t skip_tile);
 
 /*
+ * Selects the gather path of every later call in this process, for tests that
+ * must exercise one path on inputs the automatic choice would send to the
+ * other: 0 automatic (the default), 1 always the persistent tiled gather,
+ * 2 always the split gather that fhd_compute uses for small problems (one
+ * target per thread, sources split into slices across CTAs).  Results agree
+ * within the tolerance of the mode, not bit for bit, between the two paths.
+ * Returns the previous setting, or -1 (setting unchanged) for any other
+ * value.  Process-wide and not ordered with calls running in other threads.
+ * Makes no CUDA call.
+ */
+FHD_API int fhd_test_set_path(int path);
+
+/*
+ * The automatic path choice and split-gather shape for one gather of
+ * n_targets targets and n_sources sources (both >= 1) on a device with `sms`
+ * SMs running `ctas_max` persistent CTAs, with partial_bytes of partial rows
+ * in the workspace.  Returns 1 when the split gather is chosen, 0 when the
+ * persistent gather is, -1 for invalid arguments; *n_slices and *slice_len
+ * (either may be NULL) receive the split shape.  Makes no CUDA call.
+ */
+FHD_API int fhd_test_split_shape(int64_t n_targets, int64_t n_sources, int sms, int ctas_max,
+                                 size_t partial_bytes, int *n_slices, int64_t *slice_len);
+
+/*
  * Host-side replay of the gather schedule for n_targets targets, n_sources
  * sources and `ctas` persistent CTAs (capped at the number of work items),
  * using the same schedule functions as the kernels.  Returns 0 when every CTA

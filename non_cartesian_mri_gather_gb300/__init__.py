@@ -98,6 +98,9 @@ SIGNATURES = {
     "fhd_test_compute_skip_tile": (_int, [_i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _int, _vp,
                                           _sz, _vp, _i64]),
     "fhd_test_schedule": (_int, [_i64, _i64, _int]),
+    "fhd_test_set_path": (_int, [_int]),
+    "fhd_test_split_shape": (_int, [_i64, _i64, _int, _int, _sz, ctypes.POINTER(ctypes.c_int),
+                                    ctypes.POINTER(ctypes.c_int64)]),
     "fhd_test_check_array": (_int, [_vp, _sz, _int]),
 }
 

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -100,6 +101,35 @@ fhd_status check_array(const void* p, size_t bytes, size_t align, int device) {
 fhd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FHD_OK : FHD_ERR_CUDA; }
 
 // ---------------------------------------------------------------- launches
+// Path override for the test-suite (fhd_test_set_path): 0 automatic,
+// 1 always the persistent gather, 2 always the split gather.
+std::atomic<int> g_test_path{0};
+
+// Shape of the split gather for n_targets x n_sources, and whether the
+// persistent gather would leave more than half of the device's CTA thread
+// slots idle (few work items, or target blocks mostly empty), in which case
+// the split gather is used.  The slices fill about 8 CTAs of 256 threads per
+// SM, hold at least kMinSliceSources sources each, and their partial rows fit
+// the partial region of the workspace (partial_bytes).
+SplitShape split_shape(int64_t n_targets, int64_t n_sources, int sms, int ctas_max, size_t partial_bytes) {
+    constexpr int64_t kMinSliceSources = 32;
+    SplitShape r{};
+    const int64_t work = ceil_div(n_targets, kTargetsPerBlock) * ceil_div(n_sources, kTile);
+    const int64_t busy_threads =
+        std::min<int64_t>(work, ctas_max) *
+        std::min<int64_t>(kThreads, ceil_div(std::min<int64_t>(n_targets, kTargetsPerBlock), kV));
+    r.worth_it = 2 * busy_threads < (int64_t)ctas_max * kThreads;
+    const int64_t chunks = ceil_div(n_targets, kSplitThreads);
+    int64_t slices = ceil_div((int64_t)sms * 8, chunks);
+    slices = std::min(slices, ceil_div(n_sources, kMinSliceSources));
+    slices = std::min<int64_t>(slices, (int64_t)(partial_bytes / (2 * sizeof(float) * (size_t)n_targets)));
+    slices = std::min<int64_t>(slices, 65535);
+    if (slices < 2) slices = 1;
+    r.slice_len = ceil_div(n_sources, slices);
+    r.n_slices = (int)ceil_div(n_sources, r.slice_len);
+    return r;
+}
+
 fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, const Layout& L, int device,
                       cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop, int64_t skip_tile,
                       bool first_pass, const uint32_t* skip) {
@@ -133,6 +163,33 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, scale, g.n_sources, padded,
                                                 packed, status, first_pass ? 1 : 0, skip);
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
+
+    const SplitShape split = split_shape(g.n_targets, g.n_sources, sms, ctas_max, L.frho - L.partial);
+    bool use_split = split.worth_it;
+    const int forced = g_test_path.load();
+    if (forced == 1) use_split = false;
+    if (forced == 2) use_split = true;
+    if (skip_tile >= 0) use_split = false;  // the skipped tile belongs to the persistent schedule
+    if (use_split) {
+        if (ev_start && (e = cudaEventRecord(ev_start, stream)) != cudaSuccess) return FHD_ERR_CUDA;
+        const dim3 grid((unsigned)ceil_div(g.n_targets, kSplitThreads), (unsigned)split.n_slices);
+        if (fast_mode(mode))
+            split_gather_kernel<kFast><<<grid, kSplitThreads, 0, stream>>>(
+                g.tx, g.ty, g.tz, g.n_targets, packed, g.n_sources, split.slice_len, partial, g.out_r, g.out_i, skip);
+        else
+            split_gather_kernel<kAccurate><<<grid, kSplitThreads, 0, stream>>>(
+                g.tx, g.ty, g.tz, g.n_targets, packed, g.n_sources, split.slice_len, partial, g.out_r, g.out_i, skip);
+        if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
+        if (split.n_slices > 1) {
+            const int rgrid = (int)std::min<int64_t>(ceil_div(g.n_targets, 256), (int64_t)sms * 8);
+            split_reduce_kernel<<<rgrid, 256, 0, stream>>>(partial, split.n_slices, g.n_targets, g.out_r, g.out_i,
+                                                           skip);
+            if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
+        }
+        if (ev_stop && (e = cudaEventRecord(ev_stop, stream)) != cudaSuccess) return FHD_ERR_CUDA;
+        return FHD_OK;
+    }
+
     float4* desc = reinterpret_cast<float4*>(ws + L.desc);
     const int64_t n_segments = padded / kSegment;
     const int desc_grid = (int)std::min<int64_t>(ceil_div(n_segments, 256), (int64_t)sms * 8);
@@ -166,7 +223,8 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
     if (sch.ctas > 1) {
-        fixup_kernel<<<sch.ctas - 1, 256, 0, stream>>>(sch, partial, g.out_r, g.out_i, skip);
+        fixup_kernel<<<dim3(sch.ctas - 1, kFixupSplit), kFixupThreads, 0, stream>>>(sch, partial, g.out_r, g.out_i,
+                                                                                     skip);
         if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
     }
     if (ev_stop && (e = cudaEventRecord(ev_stop, stream)) != cudaSuccess) return FHD_ERR_CUDA;
@@ -445,6 +503,22 @@ fhd_status fhd_compute_noalloc(int64_t M, const float* kx, const float* ky, cons
 fhd_status fhd_test_check_array(const void* p, size_t bytes, int device) {
     if (bytes == 0) return p ? check_array(p, 4, 4, device) : FHD_ERR_INVALID_VALUE;
     return check_array(p, bytes, 4, device);
+}
+
+// Declared in include/fhd_testing.h.
+int fhd_test_set_path(int path) {
+    if (path < 0 || path > 2) return -1;
+    return g_test_path.exchange(path);
+}
+
+// Declared in include/fhd_testing.h.
+int fhd_test_split_shape(int64_t n_targets, int64_t n_sources, int sms, int ctas_max, size_t partial_bytes,
+                         int* n_slices, int64_t* slice_len) {
+    if (n_targets < 1 || n_sources < 1 || sms < 1 || ctas_max < 1) return -1;
+    const SplitShape r = split_shape(n_targets, n_sources, sms, ctas_max, partial_bytes);
+    if (n_slices) *n_slices = r.n_slices;
+    if (slice_len) *slice_len = r.slice_len;
+    return r.worth_it ? 1 : 0;
 }
 
 // Declared in include/fhd_testing.h.  Replays, on the host, the segment

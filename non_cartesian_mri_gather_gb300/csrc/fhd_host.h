@@ -49,6 +49,14 @@ struct GatherProblem {
 };
 
 Layout layout_for(fhd_op op, int64_t N, int64_t M, int sms);
+
+// Launch shape of the split gather (small problems).
+struct SplitShape {
+    bool worth_it;     // the persistent gather would leave most thread slots idle
+    int n_slices;      // source slices (grid y); 1 writes the output directly
+    int64_t slice_len; // sources per slice (the last may be shorter)
+};
+SplitShape split_shape(int64_t n_targets, int64_t n_sources, int sms, int ctas_max, size_t partial_bytes);
 fhd_status cuda_status(cudaError_t e);
 bool overlaps(const Buf& a, const Buf& b);
 fhd_status check_array(const void* p, size_t bytes, size_t align, int device);

@@ -34,6 +34,9 @@
 //   3. fixup_kernel   - target blocks whose source range was split between
 //                       CTAs are summed from per-CTA partials in a fixed
 //                       order (no atomics, bit-reproducible).
+//   Small problems, which would leave most of the persistent CTAs or threads
+//   idle, take split_gather_kernel (one target per thread, the sources split
+//   into slices across CTAs) and split_reduce_kernel instead of 2 and 3.
 //
 // Every pipeline wait is bounded by a time limit; on expiry the waiting
 // thread records an error bit in the status word and its CTA leaves early
@@ -786,25 +789,114 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
 }
 
 // ---------------------------------------------------------------- fix-up
-// One CTA per CTA boundary c = 1..ctas-1.  A boundary strictly inside target
+// kFixupSplit CTAs per CTA boundary c = 1..ctas-1, each summing one slice of
+// kTargetsPerBlock / kFixupSplit targets.  A boundary strictly inside target
 // block b means b was split; the lowest such boundary sums b's partial slots
 // over the contributing CTAs c-1 .. c_hi in increasing order.
-__global__ void fixup_kernel(const Schedule sch, const float* __restrict__ partial, float* __restrict__ out_r,
-                             float* __restrict__ out_i, const uint32_t* skip) {
+constexpr int kFixupSplit = 8;
+constexpr int kFixupThreads = 256;
+static_assert(kTargetsPerBlock % (4 * kFixupSplit) == 0, "fix-up slices are whole float4 groups");
+__global__ void __launch_bounds__(kFixupThreads) fixup_kernel(const Schedule sch, const float* __restrict__ partial,
+                                                              float* __restrict__ out_r, float* __restrict__ out_i,
+                                                              const uint32_t* skip) {
     if (skip != nullptr && *skip != 0u) return;
     const int64_t c = (int64_t)blockIdx.x + 1;
     const int64_t b = sch.fixup_block(c);
     if (b < 0) return;
     const int64_t c_lo = c - 1;
     const int64_t c_hi = sch.last_contributor(c, b);
-    for (int l = threadIdx.x; l < kTargetsPerBlock; l += blockDim.x) {
+    constexpr int kSlice = kTargetsPerBlock / kFixupSplit;
+    const int l_end = (int)(blockIdx.y + 1) * kSlice;
+    for (int l = (int)blockIdx.y * kSlice + 4 * (int)threadIdx.x; l < l_end; l += 4 * kFixupThreads) {
         const int64_t t = b * kTargetsPerBlock + l;
         if (t >= sch.n_targets) break;
-        float sr = 0.f, si = 0.f;
+        // slot rows are whole blocks, so the float4 reads stay inside the slot
+        float4 sr = make_float4(0.f, 0.f, 0.f, 0.f), si = sr;
         for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
             const float* pr = partial + sch.slot(cc, b) * (2 * kTargetsPerBlock);
-            sr += pr[l];
-            si += pr[kTargetsPerBlock + l];
+            const float4 a = *reinterpret_cast<const float4*>(pr + l);
+            const float4 q = *reinterpret_cast<const float4*>(pr + kTargetsPerBlock + l);
+            sr.x += a.x; sr.y += a.y; sr.z += a.z; sr.w += a.w;
+            si.x += q.x; si.y += q.y; si.z += q.z; si.w += q.w;
+        }
+        const float vr[4] = {sr.x, sr.y, sr.z, sr.w}, vi[4] = {si.x, si.y, si.z, si.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (t + j < sch.n_targets) {
+                out_r[t + j] = vr[j];
+                out_i[t + j] = vi[j];
+            }
+    }
+}
+
+// ---------------------------------------------------------------- split gather
+// Problems too small to occupy the persistent kernel (a few target blocks and
+// source tiles, so most CTAs or most threads would idle) take this path: one
+// target per thread, kSplitThreads targets per CTA along x, the sources split
+// into n_slices equal slices along y.  Each CTA stages its slice through
+// shared memory kSplitChunk records at a time and evaluates every pair
+// directly (one phasor per pair, as on the pair-by-pair path); a slice's sums
+// go to its own partial row, and split_reduce_kernel adds the rows in slice
+// order (no atomics, bit-reproducible).  With one slice the CTA writes the
+// output itself.
+constexpr int kSplitThreads = 256;
+constexpr int kSplitChunk = 256;
+
+template <int MODE>
+__global__ void __launch_bounds__(kSplitThreads) split_gather_kernel(
+    const float* __restrict__ tx, const float* __restrict__ ty, const float* __restrict__ tz, int64_t n_targets,
+    const float4* __restrict__ packed, int64_t n_sources, int64_t slice_len, float* __restrict__ partial,
+    float* __restrict__ out_r, float* __restrict__ out_i, const uint32_t* skip) {
+    if (skip != nullptr && *skip != 0u) return;
+    __shared__ float4 rec[2 * kSplitChunk];
+    const int64_t t = (int64_t)blockIdx.x * kSplitThreads + threadIdx.x;
+    const bool active = t < n_targets;
+    const float bx = active ? tx[t] : 0.f, by = active ? ty[t] : 0.f, bz = active ? tz[t] : 0.f;
+    const int64_t s0 = (int64_t)blockIdx.y * slice_len;
+    const int64_t s1 = s0 + slice_len < n_sources ? s0 + slice_len : n_sources;
+    float ar = 0.f, ai = 0.f;
+    for (int64_t c0 = s0; c0 < s1; c0 += kSplitChunk) {
+        const int n = (int)(s1 - c0 < kSplitChunk ? s1 - c0 : kSplitChunk);
+        __syncthreads();  // the previous chunk is consumed
+        for (int i = threadIdx.x; i < 2 * n; i += kSplitThreads) rec[i] = packed[2 * c0 + i];
+        __syncthreads();
+#pragma unroll 4
+        for (int s = 0; s < n; ++s) {
+            const float4 r0 = rec[2 * s];      // A.x A.x A.y A.y
+            const float4 r1 = rec[2 * s + 1];  // A.z A.z w.re w.im
+            const float p = fmaf(r1.x, bz, fmaf(r0.z, by, r0.x * bx));
+            float sn, cs;
+            if constexpr (MODE == kAccurate)
+                phasor_accurate(p, sn, cs);
+            else
+                phasor_mufu(p, sn, cs);
+            ar = fmaf(r1.z, cs, ar);
+            ar = fmaf(-r1.w, sn, ar);
+            ai = fmaf(r1.z, sn, ai);
+            ai = fmaf(r1.w, cs, ai);
+        }
+    }
+    if (!active) return;
+    if (gridDim.y == 1) {
+        out_r[t] = ar;
+        out_i[t] = ai;
+    } else {
+        partial[(2 * (int64_t)blockIdx.y) * n_targets + t] = ar;
+        partial[(2 * (int64_t)blockIdx.y + 1) * n_targets + t] = ai;
+    }
+}
+
+// out_t = sum over slices j = 0 .. n_slices-1, in that order, of partial row j.
+__global__ void split_reduce_kernel(const float* __restrict__ partial, int n_slices, int64_t n_targets,
+                                    float* __restrict__ out_r, float* __restrict__ out_i, const uint32_t* skip) {
+    if (skip != nullptr && *skip != 0u) return;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n_targets;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        float sr = 0.f, si = 0.f;
+#pragma unroll 8
+        for (int j = 0; j < n_slices; ++j) {
+            sr += partial[(2 * (int64_t)j) * n_targets + t];
+            si += partial[(2 * (int64_t)j + 1) * n_targets + t];
         }
         out_r[t] = sr;
         out_i[t] = si;

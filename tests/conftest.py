@@ -14,3 +14,4 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU and the compiled fhd library")
     config.addinivalue_line("markers", "slow: long-running CPU oracle case")
+    config.addinivalue_line("markers", "auto_path: GPU parity test that keeps the library's automatic path choice")

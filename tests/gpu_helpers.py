@@ -72,3 +72,26 @@ def gpu_fhf(p, mode):
     o_r, o_i = fhd.fhfrho_apply(t["x"], t["y"], t["z"], t["rho_r"], t["rho_i"], t["kx"], t["ky"], t["kz"], mode=mode)
     torch.cuda.synchronize()
     return host_complex(o_r, o_i)
+
+
+PATH_AUTO, PATH_PERSISTENT, PATH_SPLIT = 0, 1, 2
+
+
+class gather_path:
+    """Context manager: force the library's gather path (fhd_test_set_path)."""
+
+    def __init__(self, path: int):
+        self.path = path
+
+    def __enter__(self):
+        import non_cartesian_mri_gather_gb300 as fhd
+
+        self.prev = fhd.load().fhd_test_set_path(self.path)
+        assert self.prev in (0, 1, 2)
+        return self
+
+    def __exit__(self, *exc):
+        import non_cartesian_mri_gather_gb300 as fhd
+
+        fhd.load().fhd_test_set_path(self.prev)
+        return False

@@ -134,3 +134,40 @@ def test_schedule_replay(lib, ctas):
 def test_schedule_rejects_empty(lib):
     assert lib.fhd_test_schedule(0, 10, 4) != 0
     assert lib.fhd_test_schedule(10, 0, 4) != 0
+
+
+def test_set_path_hook(lib):
+    prev = lib.fhd_test_set_path(0)
+    assert prev in (0, 1, 2)
+    assert lib.fhd_test_set_path(3) == -1
+    assert lib.fhd_test_set_path(-1) == -1
+    assert lib.fhd_test_set_path(2) == 0
+    assert lib.fhd_test_set_path(prev) == 2
+
+
+# Partial rows of a workspace on a 152-SM device: 2 slots per CTA of
+# 2 x 8192 floats.
+_PARTIAL = 2 * 152 * 2 * 8192 * 4
+
+
+@pytest.mark.parametrize("nt,ns", [(1, 1), (1, 100000), (1024, 2048), (2049, 1000), (300, 31), (20000, 777),
+                                   (320000, 40), (311296, 5), (100, 40000), (8192, 2048)])
+def test_split_shape_covers_sources(lib, nt, ns):
+    """Slices cover the sources once and their partial rows fit the workspace."""
+    import ctypes
+
+    k, ln = ctypes.c_int(0), ctypes.c_int64(0)
+    assert lib.fhd_test_split_shape(nt, ns, 152, 152, _PARTIAL, ctypes.byref(k), ctypes.byref(ln)) in (0, 1)
+    assert 1 <= k.value <= 65535 and ln.value >= 1
+    assert k.value * ln.value >= ns and (k.value - 1) * ln.value < ns
+    if k.value > 1:
+        assert 2 * 4 * nt * k.value <= _PARTIAL
+        assert ln.value >= 32 or ns < 64
+
+
+def test_split_shape_choice(lib):
+    """The benchmark workloads: 32^2 x 2048 is split; the 3D ones are not."""
+    for nt, ns, want in [(1024, 2048, 1), (262144, 16384, 0), (2097152, 262144, 0), (16777216, 100000, 0),
+                         (262144, 2097152, 0), (1, 1, 1), (65536, 4096, 0), (5000, 2000, 1)]:
+        assert lib.fhd_test_split_shape(nt, ns, 152, 152, _PARTIAL, None, None) == want, (nt, ns)
+    assert lib.fhd_test_split_shape(0, 1, 152, 152, _PARTIAL, None, None) == -1

@@ -8,6 +8,12 @@ fixed spread of sampled voxels (a gather output depends only on its own voxel,
 so a sampled output is exact for that voxel), and workload 5 through its two
 passes plus properties that hold at any size.
 
+Every test here runs the persistent tiled gather (the recurrence paths, the
+split target blocks and their fix-up), also on the small sizes the automatic
+path choice sends to the split gather; the benchmark workloads run with the
+automatic choice, as the benchmark does, and workload 1 also on the persistent
+path.  The split gather has its own module (test_split_gpu.py).
+
 Tolerances: relative L2 error <= 1e-5 (accurate mode) and <= 1e-3 with
 PSNR >= 60 dB (fast mode).
 """
@@ -16,8 +22,8 @@ import pytest
 
 import oracle
 from inputs import make_workload, random_problem
-from tests.gpu_helpers import (PSNR_FAST_DB, TOL_ACCURATE, TOL_FAST, gpu_fhd, gpu_fhf, gpu_fwd, psnr_db, rel_l2,
-                               sample_indices)
+from tests.gpu_helpers import (PATH_AUTO, PATH_PERSISTENT, PSNR_FAST_DB, TOL_ACCURATE, TOL_FAST, gather_path, gpu_fhd,
+                               gpu_fhf, gpu_fwd, psnr_db, rel_l2, sample_indices)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +41,14 @@ def _lib():
     build.build()
     load()
     torch.cuda.set_device(0)
+
+
+@pytest.fixture(autouse=True)
+def _persistent_path(request):
+    """Persistent gather unless the test asks for the automatic choice."""
+    path = PATH_AUTO if "auto_path" in request.keywords else PATH_PERSISTENT
+    with gather_path(path):
+        yield
 
 
 def check(got, ref, mode, what):
@@ -95,11 +109,13 @@ def workload(i):
     return _cache[i]
 
 
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_PERSISTENT])
 @pytest.mark.parametrize("mode", ALL_MODES)
-def test_workload1_full(mode):
+def test_workload1_full(mode, path):
     p = workload(1)
     ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
-    check(gpu_fhd(p, mode), ref, mode, "workload 1")
+    with gather_path(path):
+        check(gpu_fhd(p, mode), ref, mode, f"workload 1 (path {path})")
 
 
 @pytest.fixture(scope="module")
@@ -108,11 +124,13 @@ def ref2():
     return oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
 
 
+@pytest.mark.auto_path
 @pytest.mark.parametrize("mode", ALL_MODES)
 def test_workload2_full(mode, ref2):
     check(gpu_fhd(workload(2), mode), ref2, mode, "workload 2")
 
 
+@pytest.mark.auto_path
 @pytest.mark.parametrize("wl", [3, 4])
 @pytest.mark.parametrize("mode", [ACC, FAST])
 def test_workload_sampled(wl, mode):
@@ -123,6 +141,7 @@ def test_workload_sampled(wl, mode):
     check(got[idx], ref, mode, f"workload {wl} ({idx.size} sampled voxels)")
 
 
+@pytest.mark.auto_path
 @pytest.mark.parametrize("mode", [ACC, FAST])
 def test_workload5(mode):
     """F^H F rho at 128^3 x 262144: forward pass on sampled samples vs the oracle,
