@@ -421,13 +421,6 @@ __device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, 
     }
 }
 
-// Equal-spacing recurrence.  When a thread's kV consecutive targets satisfy
-// b_v = b_0 + v*d exactly, exp(i 2 pi a.b_v) = exp(i 2 pi a.b_0) * w^v with
-// w = exp(i 2 pi a.d).  Per source the thread evaluates two phasors (b_0 and
-// d) and f = w_s * exp(i 2 pi a.b_0); every further target then costs one
-// complex multiply f *= w (4 FMA-pipe instructions) and two adds into its
-// accumulators, instead of a phase and a sin/cos per pair.  Voxels of a
-// regular image grid, and samples along a radial spoke, are equally spaced.
 // Packed pairs of float32 (low = first, high = second) for the sm_100-family
 // f32x2 instructions: one instruction does two fp32 operations, so the
 // recurrence below spends one issue slot per target per operation.
@@ -536,11 +529,17 @@ __device__ __forceinline__ bool equally_spaced(const float (&c)[kV], int n, floa
 // is equally spaced (a row of an image grid when the voxels are the sources,
 // as in the forward sum F rho).  For target b and segment sources
 // A_s = A_0 + s d: exp(i A_s.b) = e_0 u^s with e_0 = exp(i A_0.b) and
-// u = exp(i d.b).  Per (target, segment) two phasors; per source the real and
-// imaginary parts of e_s step by the three-term recurrence
-// e_{s+1} = 2 cos(d.b) e_s - e_{s-1} (two FFMA; error growth at most
-// eps * s^2 / 2 over the kSegment sources) and the complex multiply-accumulate
-// adds w_s e_s.  Targets go in groups of kDirectGroup; each group's tile sums
+// u = exp(i d.b).  Per (target, segment) one phasor, e_0, and per (target,
+// run of segments with the same step) one more, u; the real and imaginary
+// parts of e_s follow e_{s+1} = 2 cos(d.b) e_s - e_{s-1} (error growth at most
+// eps * s^2 / 2 over the kSegment sources).  As in the target-side
+// recurrence the stored terms are f_s = s_s e_s with s_s = (+, +, -, -, ...),
+// so one packed FMA steps f (coefficient -+2 cos(d.b), then + f_{s-1}).  The
+// weight is complex, so instead of a complex multiply per pair the thread
+// keeps two packed sums per target, P = sum w.re e_s and Q = sum w.im e_s
+// (the sign s_s moved onto the weights, shared by the group's targets), and
+// sum w_s e_s = (P.re - Q.im) + i (P.im + Q.re) at the end: per pair three
+// packed FMAs.  Targets go in groups of kDirectGroup; each group's tile sums
 // are folded straight into the thread's running sums.
 template <int MODE>
 __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __restrict__ rec,
@@ -550,71 +549,82 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
 #pragma unroll 1
     for (int g = 0; g < kV; g += kDirectGroup) {
         float bx[kDirectGroup], by[kDirectGroup], bz[kDirectGroup];
-        float ar[kDirectGroup], ai[kDirectGroup];
+        f2_t P[kDirectGroup], Q[kDirectGroup];
 #pragma unroll
         for (int v = 0; v < kDirectGroup; ++v) {
             bx[v] = coord[g + v][tid];
             by[v] = coord[kV + g + v][tid];
             bz[v] = coord[2 * kV + g + v][tid];
-            ar[v] = 0.f;
-            ai[v] = 0.f;
+            P[v] = 0ull;  // +0.0f in both halves
+            Q[v] = 0ull;
         }
+        // u = exp(i d.b) is evaluated only when a segment's step d differs
+        // from the previous segment's (on an image grid, once per tile)
+        float cu[kDirectGroup], su[kDirectGroup];
+        float4 d_prev = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
         for (int j = 0; j < kSegmentsPerTile; ++j) {
             const float4 b0 = rec[2 * j * kSegment];      // A_0.x A_0.x A_0.y A_0.y
             const float4 b1 = rec[2 * j * kSegment + 1];  // A_0.z A_0.z w.re w.im
             const float4 d = desc[j];
-            float er[kDirectGroup], ei[kDirectGroup], pr[kDirectGroup], pi[kDirectGroup], c2[kDirectGroup];
+            if (j == 0 || d.x != d_prev.x || d.y != d_prev.y || d.z != d_prev.z) {  // uniform over the CTA
+#pragma unroll
+                for (int v = 0; v < kDirectGroup; ++v) {
+                    const float pd = fmaf(d.z, bz[v], fmaf(d.y, by[v], d.x * bx[v]));
+                    if constexpr (MODE == kAccurate)
+                        phasor_accurate(pd, su[v], cu[v]);
+                    else
+                        phasor_mufu(pd, su[v], cu[v]);
+                }
+                d_prev = d;
+            }
+            f2_t fm[kDirectGroup], f[kDirectGroup], kpos[kDirectGroup], kneg[kDirectGroup];
 #pragma unroll
             for (int v = 0; v < kDirectGroup; ++v) {
                 const float p0 = fmaf(b1.x, bz[v], fmaf(b0.z, by[v], b0.x * bx[v]));
-                const float pd = fmaf(d.z, bz[v], fmaf(d.y, by[v], d.x * bx[v]));
-                float s0, c0, su, cu;
-                if constexpr (MODE == kAccurate) {
+                float s0, c0;
+                if constexpr (MODE == kAccurate)
                     phasor_accurate(p0, s0, c0);
-                    phasor_accurate(pd, su, cu);
-                } else {
+                else
                     phasor_mufu(p0, s0, c0);
-                    phasor_mufu(pd, su, cu);
-                }
-                pr[v] = c0;  // e_0
-                pi[v] = s0;
-                er[v] = fmaf(c0, cu, -s0 * su);  // e_1 = e_0 u
-                ei[v] = fmaf(c0, su, s0 * cu);
-                c2[v] = cu + cu;
+                fm[v] = f2_pack(c0, s0);  // f_0 = e_0
+                f[v] = f2_pack(fmaf(c0, cu[v], -s0 * su[v]), fmaf(c0, su[v], s0 * cu[v]));  // f_1 = e_0 u
+                const float c2 = cu[v] + cu[v];
+                kpos[v] = f2_pack(c2, c2);
+                kneg[v] = f2_pack(-c2, -c2);
             }
-            // source 0 uses e_0, sources 1.. use e_1, e_2, ...
+            {  // source 0 (sign +) takes f_0
+                const f2_t wr = f2_pack(b1.z, b1.z), wi = f2_pack(b1.w, b1.w);
 #pragma unroll
-            for (int v = 0; v < kDirectGroup; ++v) {
-                ar[v] = fmaf(b1.z, pr[v], ar[v]);
-                ar[v] = fmaf(-b1.w, pi[v], ar[v]);
-                ai[v] = fmaf(b1.z, pi[v], ai[v]);
-                ai[v] = fmaf(b1.w, pr[v], ai[v]);
+                for (int v = 0; v < kDirectGroup; ++v) {
+                    P[v] = f2_fma(wr, fm[v], P[v]);
+                    Q[v] = f2_fma(wi, fm[v], Q[v]);
+                }
             }
 #pragma unroll
             for (int s = 1; s < kSegment; ++s) {
                 const float4 w = rec[2 * (j * kSegment + s) + 1];  // w.re, w.im in .z, .w
+                const float sg = strided_negated(s) ? -1.f : 1.f;   // s_s, folded into the weight
+                const f2_t wr = f2_pack(sg * w.z, sg * w.z), wi = f2_pack(sg * w.w, sg * w.w);
 #pragma unroll
                 for (int v = 0; v < kDirectGroup; ++v) {
-                    ar[v] = fmaf(w.z, er[v], ar[v]);
-                    ar[v] = fmaf(-w.w, ei[v], ar[v]);
-                    ai[v] = fmaf(w.z, ei[v], ai[v]);
-                    ai[v] = fmaf(w.w, er[v], ai[v]);
+                    P[v] = f2_fma(wr, f[v], P[v]);
+                    Q[v] = f2_fma(wi, f[v], Q[v]);
                     if (s + 1 < kSegment) {
-                        const float nr = fmaf(c2[v], er[v], -pr[v]);
-                        const float ni = fmaf(c2[v], ei[v], -pi[v]);
-                        pr[v] = er[v];
-                        pi[v] = ei[v];
-                        er[v] = nr;
-                        ei[v] = ni;
+                        const f2_t fn = f2_fma((s & 1) ? kneg[v] : kpos[v], f[v], fm[v]);  // f_{s+1}
+                        fm[v] = f[v];
+                        f[v] = fn;
                     }
                 }
             }
         }
 #pragma unroll
         for (int v = 0; v < kDirectGroup; ++v) {
-            run[g + v][tid] += ar[v];
-            run[kV + g + v][tid] += ai[v];
+            float pr, pi, qr, qi;
+            f2_unpack(P[v], pr, pi);
+            f2_unpack(Q[v], qr, qi);
+            run[g + v][tid] += pr - qi;
+            run[kV + g + v][tid] += pi + qr;
         }
     }
 }

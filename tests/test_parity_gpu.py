@@ -240,7 +240,7 @@ def test_fwd_radial_spokes(mode):
 
 # ------------------------------------------------------------ source-side recurrence
 
-def _spokes(n_spokes, seed):
+def _spokes(n_spokes, seed, points=256):
     """Samples along radial spokes whose directions are multiples of 2^-12:
     every sample r*d is exact in float32, so the samples of a spoke are
     exactly equally spaced."""
@@ -248,7 +248,7 @@ def _spokes(n_spokes, seed):
     d = rng.standard_normal((n_spokes, 3))
     d /= np.linalg.norm(d, axis=1, keepdims=True)
     d = np.round(d * 4096) / 4096
-    r = np.arange(256) - 128.0
+    r = np.arange(points) - points / 2
     return (d[:, None, :] * r[None, :, None]).reshape(-1, 3).astype(np.float32)
 
 
@@ -304,6 +304,18 @@ def test_fhd_spoke_sources_random_voxels(mode):
     p.kx, p.ky, p.kz = (np.ascontiguousarray(k[:, i]) for i in range(3))
     ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
     check(gpu_fhd(p, mode), ref, mode, "F^H D spoke sources")
+
+
+@pytest.mark.parametrize("mode", ALL_MODES)
+def test_source_recurrence_step_changes_within_tile(mode):
+    """Spokes of 48 samples (three 16-source segments each): every 256-source
+    tile holds segments of several spokes, so the segment step changes inside
+    a tile and the step phasor is re-evaluated there."""
+    k = _spokes(23, 12, points=48)
+    p = random_problem(4000, k.shape[0], kmax=1.0, seed=12)
+    p.kx, p.ky, p.kz = (np.ascontiguousarray(k[:, i]) for i in range(3))
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    check(gpu_fhd(p, mode), ref, mode, "F^H D 48-sample spoke sources")
 
 
 # ------------------------------------------------------------ edge cases
