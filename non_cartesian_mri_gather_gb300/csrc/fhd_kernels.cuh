@@ -508,6 +508,55 @@ __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict
     }
 }
 
+// Accurate mode, every lane of the warp with the same target spacing d: the
+// step phasor u_s = exp(i 2 pi a_s.d) is the same for all lanes, so lane l
+// evaluates it for sources 32k + l only and the others read it by shuffle.
+// Phases and sin/cos are those of accumulate_tile_strided (pd formed in the
+// same order), so the sums are bit-identical to it, with 1/32 of the
+// sincospif calls for u.
+__device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* __restrict__ rec, float x0,
+                                                                 float y0, float z0, float dx, float dy, float dz,
+                                                                 int lane, f2_t (&acc)[kV]) {
+    static_assert(kTile % 32 == 0, "tiles hold whole warps of sources");
+#pragma unroll
+    for (int v = 0; v < kV; ++v) acc[v] = 0ull;  // +0.0f in both halves
+#pragma unroll 1
+    for (int s32 = 0; s32 < kTile; s32 += 32) {
+        float su_l, cu_l;
+        {
+            const float4 r0 = rec[2 * (s32 + lane)];
+            const float4 r1 = rec[2 * (s32 + lane) + 1];
+            phasor_accurate(fmaf(r1.y, dz, fmaf(r0.w, dy, r0.y * dx)), su_l, cu_l);
+        }
+#pragma unroll kUnroll
+        for (int q = 0; q < 32; ++q) {
+            const float4 r0 = rec[2 * (s32 + q)];      // A.x A.x A.y A.y
+            const float4 r1 = rec[2 * (s32 + q) + 1];  // A.z A.z w.re w.im
+            float s0, c0;
+            phasor_accurate(fmaf(r1.x, z0, fmaf(r0.z, y0, r0.x * x0)), s0, c0);
+            const float sw = __shfl_sync(0xffffffffu, su_l, q);
+            const float cw = __shfl_sync(0xffffffffu, cu_l, q);
+            const float fr = fmaf(r1.z, c0, -r1.w * s0);  // g_0 = w_s * exp(i 2 pi a.b_0)
+            const float fi = fmaf(r1.z, s0, r1.w * c0);
+            const float gr = fmaf(fr, cw, -fi * sw);      // g_1 = g_0 u
+            const float gi = fmaf(fr, sw, fi * cw);
+            const float c2 = cw + cw;
+            const f2_t kpos = f2_pack(c2, c2), kneg = f2_pack(-c2, -c2);
+            f2_t em = f2_pack(fr, fi);  // e_{v-1}
+            f2_t e = f2_pack(gr, gi);   // e_v
+            acc[0] = f2_add(acc[0], em);
+            acc[1] = f2_add(acc[1], e);
+#pragma unroll
+            for (int v = 1; v + 1 < kV; ++v) {
+                const f2_t en = f2_fma((v & 1) ? kneg : kpos, e, em);  // e_{v+1}
+                em = e;
+                e = en;
+                acc[v + 1] = f2_add(acc[v + 1], e);
+            }
+        }
+    }
+}
+
 // True when c[v] == c[0] + v*d exactly for the first n entries, with d the
 // float32 value c[1] - c[0] (checked in double, where these sums are exact).
 __device__ __forceinline__ bool equally_spaced(const float (&c)[kV], int n, float& d) {
@@ -693,6 +742,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
     float x0 = 0.f, y0 = 0.f, z0 = 0.f;  // first target of the thread (strided path)
     float sx = 0.f, sy = 0.f, sz = 0.f;  // target spacing of the strided path
     bool strided = false;                // warp-uniform
+    bool shared_u = false;               // strided, and every lane has the same spacing
     const int tid = threadIdx.x;
     int64_t seg_first_tile = 0;  // first tile index of the current segment
     int64_t consumed = 0;
@@ -725,7 +775,15 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
                                                              : kV);
             const bool spaced = equally_spaced(bx, n_in, sx) && equally_spaced(by, n_in, sy) &&
                                 equally_spaced(bz, n_in, sz);
-            strided = args.allow_strided && __all_sync(0xffffffffu, spaced);
+            // every lane executes every shuffle and vote (no short-circuit
+            // around a full-mask warp primitive)
+            const bool all_spaced = __all_sync(0xffffffffu, spaced);
+            const float sx0 = __shfl_sync(0xffffffffu, sx, 0);
+            const float sy0 = __shfl_sync(0xffffffffu, sy, 0);
+            const float sz0 = __shfl_sync(0xffffffffu, sz, 0);
+            const bool same_step = __all_sync(0xffffffffu, sx == sx0 && sy == sy0 && sz == sz0);
+            strided = args.allow_strided && all_spaced;
+            shared_u = strided && same_step;
         }
 
         const int st = (int)(consumed % kStages);
@@ -739,7 +797,10 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
         const float4* rec = &sm.ring[st][0];
         if (strided) {
             f2_t acc[kV];
-            accumulate_tile_strided<MODE>(rec, x0, y0, z0, sx, sy, sz, acc);
+            if (MODE == kAccurate && shared_u)
+                accumulate_tile_strided_shared_u(rec, x0, y0, z0, sx, sy, sz, lane, acc);
+            else
+                accumulate_tile_strided<MODE>(rec, x0, y0, z0, sx, sy, sz, acc);
 #pragma unroll
             for (int v = 0; v < kV; ++v) {
                 float re, im;

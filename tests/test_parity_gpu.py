@@ -198,6 +198,27 @@ def test_fhd_small_grid_rows(N, M, mode):
     check(gpu_fhd(p, mode), ref, mode, f"F^H D small grid N={N} M={M}")
 
 
+@pytest.mark.parametrize("mode", ALL_MODES)
+def test_rows_with_mixed_spacing(mode):
+    """Rows of 32 voxels, each one thread's targets, whose x spacing alternates
+    between 1/32 and 1/64 every 16 rows: every thread is equally spaced but a
+    warp's lanes differ in spacing, so the accurate recurrence evaluates the
+    step phasor per thread instead of once per warp (warps with a single
+    spacing follow further on)."""
+    rows = 320
+    i = np.arange(32)
+    xs = []
+    for r in range(rows):
+        step = 1 / 32 if (r // 16) % 2 == 0 or r >= 256 else 1 / 64
+        xs.append(-0.5 + i * step)
+    p = random_problem(32 * rows, 900, kmax=16.0, seed=14)
+    p.x = np.concatenate(xs).astype(np.float32)
+    p.y = np.repeat(((np.arange(rows) % 32) / 32 - 0.5), 32).astype(np.float32)
+    p.z = np.repeat(((np.arange(rows) // 32) / 16 - 0.5), 32).astype(np.float32)
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    check(gpu_fhd(p, mode), ref, mode, "F^H D mixed row spacing")
+
+
 @pytest.mark.parametrize("mode", [ACC, FAST])
 def test_perturbed_grid_falls_back(mode):
     """One voxel moved by one float32 ulp breaks the exact spacing of its row:
