@@ -113,6 +113,10 @@ def parse():
     ap.add_argument("--ladder", action="store_true",
                     help="time the case study's optimisation ladder (include/fhd_ladder.h) next to the library "
                          "on workloads 1 and 2 instead of the benchmark line (one JSON line per variant)")
+    ap.add_argument("--cg", type=int, default=0, metavar="ITERS",
+                    help="time ITERS conjugate-gradient iterations (fhd_cg_solve, tolerance 0) on the workload's "
+                         "geometry instead of the benchmark line (one JSON line)")
+    ap.add_argument("--lam", type=float, default=0.0, help="Tikhonov weight lambda of --cg")
     return ap.parse_args()
 
 
@@ -565,10 +569,69 @@ def run_ladder(args):
                               "rel_l2_vs_naive": rel}), flush=True)
 
 
+def run_cg(args):
+    """One JSON line: args.cg iterations of fhd_cg_solve on the workload's
+    voxels and samples, timed with CUDA events around the whole solve (b =
+    F^H D, then per iteration one F^H F p and the vector updates) after
+    args.warmup untimed solves, median of args.steps solves.  The data D are
+    the workload's k-space data; for workload 5 (an image workload) D = F rho
+    of its phantom (accurate mode), so the solve should approach that image.
+    Pairs per solve: N M for b plus 2 N M per iteration."""
+    import torch
+
+    import non_cartesian_mri_gather_gb300 as fhd
+
+    fhd.load()
+    mode = {"fast": fhd.MODE_FAST, "accurate": fhd.MODE_ACCURATE, "fast-direct": fhd.MODE_FAST_DIRECT,
+            "accurate-direct": fhd.MODE_ACCURATE_DIRECT}[args.mode]
+    p = load_workload(args.workload)
+    dev = torch.device("cuda", 0)
+    names = ("x", "y", "z", "kx", "ky", "kz") + (("rho_r", "rho_i") if p.op == "fhf" else ("Dr", "Di"))
+    d = {k: torch.from_numpy(getattr(p, k)).to(dev) for k in names}
+    if p.op == "fhf":
+        Dr, Di = fhd.fwd_compute(d["x"], d["y"], d["z"], d["rho_r"], d["rho_i"], d["kx"], d["ky"], d["kz"],
+                                 mode=fhd.MODE_ACCURATE)
+    else:
+        Dr, Di = d["Dr"], d["Di"]
+    ws = fhd.CgWorkspace(p.N, p.M)
+
+    def solve(info=False):
+        return fhd.fhd_cg_solve(d["kx"], d["ky"], d["kz"], Dr, Di, d["x"], d["y"], d["z"], lam=args.lam,
+                                max_iter=args.cg, tol=0.0, mode=mode, workspace=ws, info=info)
+
+    for _ in range(args.warmup):
+        solve()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(max(1, args.steps)):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        solve()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = float(np.median(times))
+    rr, ri, (iters, rs, stopped) = solve(info=True)
+    pairs = p.N * p.M * (1 + 2 * iters)
+    line = {"metric": "CG solve voxel-sample pairs/s", "value": pairs / (ms * 1e-3), "unit": "pairs/s",
+            "ms_per_solve": ms, "iterations": iters, "ms_per_iteration": ms / max(iters, 1), "rs_final": rs,
+            "stopped": stopped, "lambda": args.lam, "mode": args.mode, "steps": len(times), "warmup": args.warmup,
+            "config": {"workload": WORKLOAD_NAMES[args.workload], "N": p.N, "M": p.M,
+                       "data": "F rho of the phantom" if p.op == "fhf" else "the workload's k-space data"}}
+    if p.op == "fhf":
+        got = torch.complex(rr.double(), ri.double()).cpu().numpy()
+        truth = p.rho_r.astype(np.float64) + 1j * p.rho_i
+        line["rel_to_phantom"] = float(np.linalg.norm(got - truth) / np.linalg.norm(truth))
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.ladder:
         run_ladder(args)
+        return
+    if args.cg:
+        run_cg(args)
         return
     world, rank, local = dist_init()
     try:
