@@ -181,9 +181,8 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
                 g.tx, g.ty, g.tz, g.n_targets, packed, g.n_sources, split.slice_len, partial, g.out_r, g.out_i, skip);
         if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
         if (split.n_slices > 1) {
-            const int rgrid = (int)std::min<int64_t>(ceil_div(g.n_targets, 256), (int64_t)sms * 8);
-            split_reduce_kernel<<<rgrid, 256, 0, stream>>>(partial, split.n_slices, g.n_targets, g.out_r, g.out_i,
-                                                           skip);
+            split_reduce_kernel<<<(unsigned)ceil_div(g.n_targets, 32), 32 * kReduceWarps, 0, stream>>>(
+                partial, split.n_slices, g.n_targets, g.out_r, g.out_i, skip);
             if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
         }
         if (ev_stop && (e = cudaEventRecord(ev_stop, stream)) != cudaSuccess) return FHD_ERR_CUDA;

@@ -907,7 +907,7 @@ __global__ void __launch_bounds__(kFixupThreads) fixup_kernel(const Schedule sch
 // into n_slices equal slices along y.  Each CTA stages its slice through
 // shared memory kSplitChunk records at a time and evaluates every pair
 // directly (one phasor per pair, as on the pair-by-pair path); a slice's sums
-// go to its own partial row, and split_reduce_kernel adds the rows in slice
+// go to its own partial row, and split_reduce_kernel adds the rows in a fixed
 // order (no atomics, bit-reproducible).  With one slice the CTA writes the
 // output itself.
 constexpr int kSplitThreads = 256;
@@ -957,20 +957,38 @@ __global__ void __launch_bounds__(kSplitThreads) split_gather_kernel(
     }
 }
 
-// out_t = sum over slices j = 0 .. n_slices-1, in that order, of partial row j.
-__global__ void split_reduce_kernel(const float* __restrict__ partial, int n_slices, int64_t n_targets,
-                                    float* __restrict__ out_r, float* __restrict__ out_i, const uint32_t* skip) {
+// out_t = sum over slices of partial row j, in a fixed order: 32 targets per
+// CTA (one per lane); warp w adds slices w, w + kReduceWarps, ... in
+// increasing order, then the kReduceWarps warp sums are added in warp order
+// (no atomics, bit-reproducible).
+constexpr int kReduceWarps = 8;
+__global__ void __launch_bounds__(32 * kReduceWarps)
+    split_reduce_kernel(const float* __restrict__ partial, int n_slices, int64_t n_targets,
+                        float* __restrict__ out_r, float* __restrict__ out_i, const uint32_t* skip) {
     if (skip != nullptr && *skip != 0u) return;
-    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n_targets;
-         t += (int64_t)gridDim.x * blockDim.x) {
-        float sr = 0.f, si = 0.f;
-#pragma unroll 8
-        for (int j = 0; j < n_slices; ++j) {
+    __shared__ float wr[kReduceWarps][32], wi[kReduceWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t = (int64_t)blockIdx.x * 32 + lane;
+    float sr = 0.f, si = 0.f;
+    if (t < n_targets) {
+#pragma unroll 4
+        for (int j = warp; j < n_slices; j += kReduceWarps) {
             sr += partial[(2 * (int64_t)j) * n_targets + t];
             si += partial[(2 * (int64_t)j + 1) * n_targets + t];
         }
-        out_r[t] = sr;
-        out_i[t] = si;
+    }
+    wr[warp][lane] = sr;
+    wi[warp][lane] = si;
+    __syncthreads();
+    if (warp == 0 && t < n_targets) {
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int w = 0; w < kReduceWarps; ++w) {
+            a += wr[w][lane];
+            b += wi[w][lane];
+        }
+        out_r[t] = a;
+        out_i[t] = b;
     }
 }
 

@@ -3,7 +3,7 @@
 When a problem has too few target blocks and source tiles to occupy the
 persistent gather, fhd_compute (and the forward pass) evaluate every pair
 directly with one target per thread and the sources split into slices across
-CTAs, then add the slices' partial rows in slice order.  These tests force
+CTAs, then add the slices' partial rows in a fixed order.  These tests force
 that path (fhd_test_set_path) on sizes spanning one and many slices, ragged
 target chunks and slices, one source, one target and the single-slice case
 that writes the output directly, and compare every output with the fp64
