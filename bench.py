@@ -19,9 +19,10 @@ roofline   the gather kernel against its plain-ALU bound
            128 FP32 lanes, 16 MUFU lanes and 4 schedulers issuing one warp
            instruction (32 lanes) per clock, per SM; n_fma, n_mufu and n_issue
            are the algorithm's FP32 lane operations, MUFU operations and
-           instructions per pair.  Pair by pair (direct): 7, 2, 9 (k.x and the
-           complex MAC; sin, cos).  Equal-spacing recurrence on the benchmark's
-           grid voxels, V = 32 targets per thread, packed f32x2 arithmetic:
+           instructions per pair.  Pair by pair (direct): 7 + 13/16,
+           2 * 15/16, 9 + 11/16 (k.x and the complex MAC; sin, cos on the
+           MUFU pipe for 15 of 16 pairs, an FMA-pipe polynomial for the 16th).
+           Equal-spacing recurrence on the benchmark's grid voxels, V = 32 targets per thread, packed f32x2 arithmetic:
            per target one packed add and (from the third target on) one packed
            three-term step, plus per (thread, sample) the two phases (3 packed
            instructions), D*exp(i theta_0) (4), its first step (4),
@@ -65,8 +66,12 @@ def per_pair_counts(path: str):
     the algorithm on `path` (all three count what the algorithm needs, not what
     the compiler emits)."""
     if path == "direct":
-        # k.x (1 FMUL + 2 FFMA) + complex MAC (4 FFMA); sin, cos
-        return 7.0, 2.0, 9.0
+        # k.x (1 FMUL + 2 FFMA) + complex MAC (4 FFMA); sin, cos on the MUFU
+        # pipe for 15 of every 16 pairs, and for the 16th the FMA-pipe
+        # polynomial (reduction 3, half-angle square 1, S and C 7, sin and
+        # cos 2: 13 lane operations)
+        g = 16.0
+        return 7.0 + 13.0 / g, 2.0 * (g - 1) / g, 9.0 - 2.0 / g + 13.0 / g
     if path == "source":
         # source-side recurrence, segments of S = 16 sources, groups of G = 8
         # targets, packed f32x2: per pair one packed three-term step and two

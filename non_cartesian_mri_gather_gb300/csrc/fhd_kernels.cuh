@@ -100,15 +100,32 @@ constexpr uint32_t kStatusProducerTimeout = 2u;
 constexpr uint32_t kStatusDrainTimeout = 4u;
 
 enum Mode : int { kAccurate = 0, kFast = 1 };
-// The pair-by-pair path walks a thread's kV targets in groups of kDirectGroup
-// (coordinates of one group in registers at a time).
+// The pair-by-pair path walks a thread's kV targets in groups (coordinates and
+// per-tile sums of one group in registers at a time): wider in fast mode,
+// where more independent MUFU operations per warp hide their latency, than in
+// accurate mode, whose sincospif needs the registers.
 #ifndef FHD_DIRECT_GROUP
-#define FHD_DIRECT_GROUP 8
+#define FHD_DIRECT_GROUP 16
 #endif
-constexpr int kDirectGroup = kV < FHD_DIRECT_GROUP ? kV : FHD_DIRECT_GROUP;
-static_assert(kV % kDirectGroup == 0, "kV must be a multiple of the direct-path group");
-constexpr int kFastPolySlots = FHD_FAST_POLY_SLOTS;  // of kDirectGroup: share of sin/cos on the FMA pipe
-static_assert(kFastPolySlots >= 0 && kFastPolySlots <= kDirectGroup, "bad polynomial split");
+#ifndef FHD_DIRECT_GROUP_ACCURATE
+#define FHD_DIRECT_GROUP_ACCURATE 8
+#endif
+template <int MODE>
+__host__ __device__ constexpr int direct_group() {
+    return (MODE == kAccurate ? FHD_DIRECT_GROUP_ACCURATE : FHD_DIRECT_GROUP) < kV
+               ? (MODE == kAccurate ? FHD_DIRECT_GROUP_ACCURATE : FHD_DIRECT_GROUP)
+               : kV;
+}
+static_assert(kV % direct_group<kFast>() == 0 && kV % direct_group<kAccurate>() == 0,
+              "kV must be a multiple of the direct-path groups");
+constexpr int kFastPolySlots = FHD_FAST_POLY_SLOTS;  // of a fast group: share of sin/cos on the FMA pipe
+static_assert(kFastPolySlots >= 0 && kFastPolySlots <= direct_group<kFast>(), "bad polynomial split");
+// The source-side recurrence walks a thread's targets in groups of kSourceGroup.
+#ifndef FHD_SOURCE_GROUP
+#define FHD_SOURCE_GROUP 8
+#endif
+constexpr int kSourceGroup = kV < FHD_SOURCE_GROUP ? kV : FHD_SOURCE_GROUP;
+static_assert(kV % kSourceGroup == 0, "kV must be a multiple of the source-recurrence group");
 
 
 // Static schedule shared by the gather and fix-up kernels (and by the
@@ -345,25 +362,23 @@ struct __align__(16) GatherSmem {
     float run[2 * kV][kThreads];
     // Target coordinates of the current segment, one private column per
     // consumer thread (rows: x, y, z of each of the kV targets).  The
-    // pair-by-pair path re-reads kDirectGroup targets' coordinates per tile;
+    // pair-by-pair path re-reads one group of targets' coordinates per tile;
     // the recurrence needs only b_0 and d, which stay in registers.
     float coord[3 * kV][kThreads];
     uint64_t full[kStages];
     uint64_t empty[kStages];
 };
 
-// Sum of one staged tile into fresh per-tile accumulators tr, ti: every
-// record is read by all lanes at once (broadcast) and combined with the
-// thread's kV targets.  In fast mode the last NPOLY register slots take the
-// FMA-pipe polynomial, the others the MUFU pipe.
+// Sum of one staged tile over the thread's kV targets, pair by pair: every
+// record is read by all lanes at once (broadcast).  Targets go in groups of
+// direct_group<MODE>() with fresh per-tile accumulators; each group's tile sums are
+// folded into the thread's running sums in shared memory.  In fast mode the
+// last NPOLY slots of a group take the FMA-pipe polynomial, the others the
+// MUFU pipe.
 template <int MODE, int NPOLY>
 __device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, const float (*coord)[kThreads],
-                                                int tid, float (&tr)[kV], float (&ti)[kV]) {
-#pragma unroll
-    for (int v = 0; v < kV; ++v) {
-        tr[v] = 0.f;
-        ti[v] = 0.f;
-    }
+                                                float (*run)[kThreads], int tid) {
+    constexpr int kDirectGroup = direct_group<MODE>();
 #pragma unroll 1
     for (int g = 0; g < kV; g += kDirectGroup) {
         float bx[kDirectGroup], by[kDirectGroup], bz[kDirectGroup];
@@ -402,21 +417,8 @@ __device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, 
         }
 #pragma unroll
         for (int v = 0; v < kDirectGroup; ++v) {
-            if (g == 0) {  // the group loop is not unrolled: select into fixed registers
-                tr[v] = gr[v];
-                ti[v] = gi[v];
-            }
-        }
-        if constexpr (kV > kDirectGroup) {
-#pragma unroll
-            for (int gg = kDirectGroup; gg < kV; gg += kDirectGroup)
-                if (g == gg) {
-#pragma unroll
-                    for (int v = 0; v < kDirectGroup; ++v) {
-                        tr[gg + v] = gr[v];
-                        ti[gg + v] = gi[v];
-                    }
-                }
+            run[g + v][tid] += gr[v];
+            run[kV + g + v][tid] += gi[v];
         }
     }
 }
@@ -557,6 +559,31 @@ __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* _
     }
 }
 
+// One staged tile on the target-side recurrence, folded into the thread's
+// running sums (the signs of the stored terms undone here).
+template <int MODE>
+__device__ __forceinline__ void strided_tile(const float4* __restrict__ rec, float x0, float y0, float z0,
+                                             float dx, float dy, float dz, int lane, bool shared_u,
+                                             float (*run)[kThreads], int tid) {
+    f2_t acc[kV];
+    if (MODE == kAccurate && shared_u)
+        accumulate_tile_strided_shared_u(rec, x0, y0, z0, dx, dy, dz, lane, acc);
+    else
+        accumulate_tile_strided<MODE>(rec, x0, y0, z0, dx, dy, dz, acc);
+#pragma unroll
+    for (int v = 0; v < kV; ++v) {
+        float re, im;
+        f2_unpack(acc[v], re, im);
+        if (strided_negated(v)) {
+            run[v][tid] -= re;
+            run[kV + v][tid] -= im;
+        } else {
+            run[v][tid] += re;
+            run[kV + v][tid] += im;
+        }
+    }
+}
+
 // True when c[v] == c[0] + v*d exactly for the first n entries, with d the
 // float32 value c[1] - c[0] (checked in double, where these sums are exact).
 __device__ __forceinline__ bool equally_spaced(const float (&c)[kV], int n, float& d) {
@@ -588,7 +615,7 @@ __device__ __forceinline__ bool equally_spaced(const float (&c)[kV], int n, floa
 // keeps two packed sums per target, P = sum w.re e_s and Q = sum w.im e_s
 // (the sign s_s moved onto the weights, shared by the group's targets), and
 // sum w_s e_s = (P.re - Q.im) + i (P.im + Q.re) at the end: per pair three
-// packed FMAs.  Targets go in groups of kDirectGroup; each group's tile sums
+// packed FMAs.  Targets go in groups of kSourceGroup; each group's tile sums
 // are folded straight into the thread's running sums.
 template <int MODE>
 __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __restrict__ rec,
@@ -596,11 +623,11 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
                                                             const float (*coord)[kThreads], float (*run)[kThreads],
                                                             int tid) {
 #pragma unroll 1
-    for (int g = 0; g < kV; g += kDirectGroup) {
-        float bx[kDirectGroup], by[kDirectGroup], bz[kDirectGroup];
-        f2_t P[kDirectGroup], Q[kDirectGroup];
+    for (int g = 0; g < kV; g += kSourceGroup) {
+        float bx[kSourceGroup], by[kSourceGroup], bz[kSourceGroup];
+        f2_t P[kSourceGroup], Q[kSourceGroup];
 #pragma unroll
-        for (int v = 0; v < kDirectGroup; ++v) {
+        for (int v = 0; v < kSourceGroup; ++v) {
             bx[v] = coord[g + v][tid];
             by[v] = coord[kV + g + v][tid];
             bz[v] = coord[2 * kV + g + v][tid];
@@ -609,7 +636,7 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
         }
         // u = exp(i d.b) is evaluated only when a segment's step d differs
         // from the previous segment's (on an image grid, once per tile)
-        float cu[kDirectGroup], su[kDirectGroup];
+        float cu[kSourceGroup], su[kSourceGroup];
         float4 d_prev = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
         for (int j = 0; j < kSegmentsPerTile; ++j) {
@@ -618,7 +645,7 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
             const float4 d = desc[j];
             if (j == 0 || d.x != d_prev.x || d.y != d_prev.y || d.z != d_prev.z) {  // uniform over the CTA
 #pragma unroll
-                for (int v = 0; v < kDirectGroup; ++v) {
+                for (int v = 0; v < kSourceGroup; ++v) {
                     const float pd = fmaf(d.z, bz[v], fmaf(d.y, by[v], d.x * bx[v]));
                     if constexpr (MODE == kAccurate)
                         phasor_accurate(pd, su[v], cu[v]);
@@ -627,9 +654,9 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
                 }
                 d_prev = d;
             }
-            f2_t fm[kDirectGroup], f[kDirectGroup], kpos[kDirectGroup], kneg[kDirectGroup];
+            f2_t fm[kSourceGroup], f[kSourceGroup], kpos[kSourceGroup], kneg[kSourceGroup];
 #pragma unroll
-            for (int v = 0; v < kDirectGroup; ++v) {
+            for (int v = 0; v < kSourceGroup; ++v) {
                 const float p0 = fmaf(b1.x, bz[v], fmaf(b0.z, by[v], b0.x * bx[v]));
                 float s0, c0;
                 if constexpr (MODE == kAccurate)
@@ -645,7 +672,7 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
             {  // source 0 (sign +) takes f_0
                 const f2_t wr = f2_pack(b1.z, b1.z), wi = f2_pack(b1.w, b1.w);
 #pragma unroll
-                for (int v = 0; v < kDirectGroup; ++v) {
+                for (int v = 0; v < kSourceGroup; ++v) {
                     P[v] = f2_fma(wr, fm[v], P[v]);
                     Q[v] = f2_fma(wi, fm[v], Q[v]);
                 }
@@ -656,7 +683,7 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
                 const float sg = strided_negated(s) ? -1.f : 1.f;   // s_s, folded into the weight
                 const f2_t wr = f2_pack(sg * w.z, sg * w.z), wi = f2_pack(sg * w.w, sg * w.w);
 #pragma unroll
-                for (int v = 0; v < kDirectGroup; ++v) {
+                for (int v = 0; v < kSourceGroup; ++v) {
                     P[v] = f2_fma(wr, f[v], P[v]);
                     Q[v] = f2_fma(wi, f[v], Q[v]);
                     if (s + 1 < kSegment) {
@@ -668,7 +695,7 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
             }
         }
 #pragma unroll
-        for (int v = 0; v < kDirectGroup; ++v) {
+        for (int v = 0; v < kSourceGroup; ++v) {
             float pr, pi, qr, qi;
             f2_unpack(P[v], pr, pi);
             f2_unpack(Q[v], qr, qi);
@@ -676,6 +703,25 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
             run[kV + g + v][tid] += pi + qr;
         }
     }
+}
+
+// Out-of-line entry points of the pair-by-pair and source-side paths.  The
+// gather kernel is one function holding all three paths, and the register
+// allocation and scheduling of its hot loop depend on what else is inlined
+// into it: measured on the 256^3 x 100000 grid, the accurate kernel runs its
+// recurrence fastest with these two paths called out of line, the fast kernel
+// with everything inlined.
+template <int MODE, int NPOLY>
+__device__ __noinline__ void accumulate_tile_ool(const float4* __restrict__ rec, const float (*coord)[kThreads],
+                                                 float (*run)[kThreads], int tid) {
+    accumulate_tile<MODE, NPOLY>(rec, coord, run, tid);
+}
+template <int MODE>
+__device__ __noinline__ void accumulate_tile_src_strided_ool(const float4* __restrict__ rec,
+                                                             const float4* __restrict__ desc,
+                                                             const float (*coord)[kThreads],
+                                                             float (*run)[kThreads], int tid) {
+    accumulate_tile_src_strided<MODE>(rec, desc, coord, run, tid);
 }
 
 // MODE: kAccurate or kFast.  NPOLY (fast mode only): how many of the kV
@@ -796,21 +842,25 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
         // O(sqrt(kTile) + sqrt(M / kTile)) instead of O(sqrt(M)).
         const float4* rec = &sm.ring[st][0];
         if (strided) {
-            f2_t acc[kV];
-            if (MODE == kAccurate && shared_u)
-                accumulate_tile_strided_shared_u(rec, x0, y0, z0, sx, sy, sz, lane, acc);
-            else
-                accumulate_tile_strided<MODE>(rec, x0, y0, z0, sx, sy, sz, acc);
+            if constexpr (MODE == kFast) {
+                strided_tile<MODE>(rec, x0, y0, z0, sx, sy, sz, lane, shared_u, sm.run, tid);
+            } else {
+                f2_t acc[kV];
+                if (shared_u)
+                    accumulate_tile_strided_shared_u(rec, x0, y0, z0, sx, sy, sz, lane, acc);
+                else
+                    accumulate_tile_strided<MODE>(rec, x0, y0, z0, sx, sy, sz, acc);
 #pragma unroll
-            for (int v = 0; v < kV; ++v) {
-                float re, im;
-                f2_unpack(acc[v], re, im);
-                if (strided_negated(v)) {
-                    sm.run[v][tid] -= re;
-                    sm.run[kV + v][tid] -= im;
-                } else {
-                    sm.run[v][tid] += re;
-                    sm.run[kV + v][tid] += im;
+                for (int v = 0; v < kV; ++v) {
+                    float re, im;
+                    f2_unpack(acc[v], re, im);
+                    if (strided_negated(v)) {
+                        sm.run[v][tid] -= re;
+                        sm.run[kV + v][tid] -= im;
+                    } else {
+                        sm.run[v][tid] += re;
+                        sm.run[kV + v][tid] += im;
+                    }
                 }
             }
         } else {
@@ -818,15 +868,15 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
 #pragma unroll
             for (int q = 0; q < kSegmentsPerTile; ++q) src_strided = src_strided && sm.desc[st][q].w != 0.f;
             if (src_strided) {
-                accumulate_tile_src_strided<MODE>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
+                if constexpr (MODE == kFast)
+                    accumulate_tile_src_strided<MODE>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
+                else
+                    accumulate_tile_src_strided_ool<MODE>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
             } else {
-                float tr[kV], ti[kV];
-                accumulate_tile<MODE, NPOLY>(rec, sm.coord, tid, tr, ti);
-#pragma unroll
-                for (int v = 0; v < kV; ++v) {
-                    sm.run[v][tid] += tr[v];
-                    sm.run[kV + v][tid] += ti[v];
-                }
+                if constexpr (MODE == kFast)
+                    accumulate_tile<MODE, NPOLY>(rec, sm.coord, sm.run, tid);
+                else
+                    accumulate_tile_ool<MODE, NPOLY>(rec, sm.coord, sm.run, tid);
             }
         }
         __syncwarp();

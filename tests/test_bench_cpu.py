@@ -22,14 +22,17 @@ def test_defaults(monkeypatch):
 
 
 def test_roofline_counts():
-    # pair by pair: the MUFU pipe binds, 16 / 2 = 8 pairs per SM per clock
-    assert bench.per_pair_counts("direct") == (7.0, 2.0, 9.0)
-    assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct") - 152 * 8 * 2070e6) < 1
+    # pair by pair: the MUFU pipe binds; 15 of 16 pairs take sin and cos on
+    # it, so 16 / (2 * 15/16) = 8.53 pairs per SM per clock
+    lanes, mufu, issue = bench.per_pair_counts("direct")
+    assert (lanes, mufu, issue) == (7 + 13 / 16, 2 * 15 / 16, 9 - 2 / 16 + 13 / 16)
+    assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct") - 152 * (16 / mufu) * 2070e6) < 1
+    assert 16 / mufu < min(128 / lanes, 128 / issue)
     lanes, mufu, issue = bench.per_pair_counts("recurrence")
     V = bench.TARGETS_PER_THREAD
     assert abs(lanes - (4 - 4 / V + 15 / V)) < 1e-12 and abs(mufu - 4 / V) < 1e-12
     assert abs(issue - (2 + 14 / V)) < 1e-12
-    # with V = 16 the FP32 lanes bind
+    # with V = 32 the FP32 lanes bind
     assert abs(bench.peak_pairs_per_s(152, 2070.0, "recurrence") - 152 * (128 / lanes) * 2070e6) < 1
 
 
