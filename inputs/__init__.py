@@ -103,6 +103,33 @@ def grid_coords(nx: int, ny: int, nz: int = 1):
     return _f32(x.ravel()), _f32(y.ravel()), _f32(z.ravel())
 
 
+def grid_coords_at(idx, nx: int, ny: int, nz: int):
+    """The coordinates ``grid_coords(nx, ny, nz)`` holds at linear indices
+    ``idx`` (int64 array), without building the whole grid."""
+    idx = np.asarray(idx, dtype=np.int64)
+    x = -0.5 + (idx % nx).astype(np.float64) / nx
+    y = -0.5 + ((idx // nx) % ny).astype(np.float64) / ny
+    z = (-0.5 + (idx // (nx * ny)).astype(np.float64) / nz) if nz > 1 else np.zeros(idx.shape)
+    return _f32(x), _f32(y), _f32(z)
+
+
+def grid_coords_device(n: int, nx: int, ny: int, nz: int, device, chunk: int = 1 << 26):
+    """The first n points of ``grid_coords(nx, ny, nz)`` as float32 torch
+    tensors built directly on `device`, a chunk of indices at a time, for
+    grids too large to build on the host.  Power-of-two sides keep every
+    coordinate exact, equal to ``grid_coords_at``."""
+    import torch
+
+    out = [torch.empty(n, dtype=torch.float32, device=device) for _ in range(3)]
+    for c0 in range(0, n, chunk):
+        i = torch.arange(c0, min(n, c0 + chunk), dtype=torch.int64, device=device)
+        out[0][c0:c0 + i.numel()] = (-0.5 + (i % nx).double() / nx).float()
+        out[1][c0:c0 + i.numel()] = (-0.5 + ((i // nx) % ny).double() / ny).float()
+        out[2][c0:c0 + i.numel()] = ((-0.5 + (i // (nx * ny)).double() / nz).float() if nz > 1
+                                     else torch.zeros(i.numel(), device=device))
+    return out
+
+
 def spiral_2d(interleaves: int = 4, points: int = 512, kmax: float = 16.0, turns: float = 4.0):
     """Archimedean multi-interleave spiral in the kx-ky plane (kz = 0).
 

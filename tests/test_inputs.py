@@ -101,3 +101,19 @@ def test_page_work_size():
     pairs = 256 ** 3 * 100000
     assert abs(pairs - vals["pairs_256cube_100k"]) / vals["pairs_256cube_100k"] < 0.05
     assert abs(50 * pairs - vals["pairs_cg50"]) / vals["pairs_cg50"] < 0.05
+
+
+def test_grid_coords_at_and_device_match_the_grid():
+    import torch
+
+    from inputs import grid_coords, grid_coords_at, grid_coords_device
+
+    full = grid_coords(16, 8, 4)
+    idx = np.array([0, 1, 15, 16, 127, 128, 511, 300])
+    for a, b in zip(grid_coords_at(idx, 16, 8, 4), full):
+        assert np.array_equal(a, b[idx])
+    dev = grid_coords_device(500, 16, 8, 4, "cpu", chunk=37)
+    for a, b in zip(dev, full):
+        assert np.array_equal(a.numpy(), b[:500])
+    for a, b in zip(grid_coords_device(100, 16, 8, 1, "cpu"), grid_coords(16, 8, 1)):
+        assert np.array_equal(a.numpy(), b[:100])
