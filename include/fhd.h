@@ -59,9 +59,14 @@
  *            an exact identity evaluated in fp32 (same tolerances).  Other
  *            targets are evaluated pair by pair.  Likewise, where runs of
  *            16 consecutive sources are exactly equally spaced (the voxels of
- *            a grid row as sources of F rho), each target evaluates two
- *            phasors per run and steps the rest by the same recurrence.  FHD_MODE_DIRECT forces the
+ *            a grid row as sources of F rho), each target evaluates one
+ *            phasor per run (two when the run's step changes) and steps the
+ *            rest by the same recurrence.  FHD_MODE_DIRECT forces the
  *            pair-by-pair evaluation everywhere.
+ * Small      problems too small to occupy the persistent kernel (a few blocks
+ *            of 8192 targets times a few tiles of 256 sources) are evaluated
+ *            pair by pair with one target per thread and the sources split
+ *            into slices across CTAs; the slices are added in a fixed order.
  * Results are bit-identical from run to run on the same device: the sample
  * dimension is split among CTAs in a fixed way and the partial sums are
  * added in a fixed order, without atomics.
@@ -116,7 +121,8 @@ typedef enum {
  * Workspace size in bytes that `op` needs for N voxels and M samples on CUDA
  * device `device` (it depends on the device's SM count).  Returns 0 for an
  * invalid op, negative sizes or an unknown device.  The same workspace may be
- * reused by later calls on the same stream.
+ * reused by later calls on the same stream; calls that may run at the same
+ * time (on different streams) need separate workspaces.
  */
 FHD_API size_t fhd_workspace_bytes(fhd_op op, int64_t N, int64_t M, int device);
 
