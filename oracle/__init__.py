@@ -79,6 +79,8 @@ class Oracle:
             fn.restype = None
             fn.argtypes = [ctypes.c_int64, _D, _D, _D, _D, _D, ctypes.c_int64, _D, _D, _D, _D, _D]
         self._lib.oracle_threads.restype = ctypes.c_int
+        self._lib.oracle_set_threads.restype = ctypes.c_int
+        self._lib.oracle_set_threads.argtypes = [ctypes.c_int]
         self._lib.oracle_mutant_id.restype = ctypes.c_int
         assert self._lib.oracle_mutant_id() == mutant
 
@@ -92,6 +94,10 @@ class Oracle:
 
     def threads(self) -> int:
         return int(self._lib.oracle_threads())
+
+    def set_threads(self, n: int) -> int:
+        """Thread count of later calls; returns the previous one."""
+        return int(self._lib.oracle_set_threads(int(n)))
 
     def adjoint(self, kx, ky, kz, D, x, y, z) -> np.ndarray:
         """rho_n = sum_m D_m exp(+i 2 pi k_m . x_n); D complex (or (Dr, Di))."""

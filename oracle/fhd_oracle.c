@@ -151,4 +151,19 @@ int oracle_threads(void)
 #endif
 }
 
+/* Sets the OpenMP thread count of later calls (no effect without OpenMP);
+ * the benchmark uses it to time the oracle on one core as well as on all.
+ * Returns the previous count. */
+int oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    const int prev = omp_get_max_threads();
+    if (n > 0) omp_set_num_threads(n);
+    return prev;
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }
