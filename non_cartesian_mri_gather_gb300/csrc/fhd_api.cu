@@ -190,9 +190,14 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     }
 
     float4* desc = reinterpret_cast<float4*>(ws + L.desc);
-    const int64_t n_segments = padded / kSegment;
+    const int64_t n_segments = padded / (fast_mode(mode) ? segment_len<kFast>() : segment_len<kAccurate>());
     const int desc_grid = (int)std::min<int64_t>(ceil_div(n_segments, 256), (int64_t)sms * 8);
-    describe_segments<<<desc_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, scale, g.n_sources, n_segments, desc, skip);
+    if (fast_mode(mode))
+        describe_segments<segment_len<kFast>()><<<desc_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, scale, g.n_sources,
+                                                                                 n_segments, desc, skip);
+    else
+        describe_segments<segment_len<kAccurate>()><<<desc_grid, 256, 0, stream>>>(
+            g.sx, g.sy, g.sz, scale, g.n_sources, n_segments, desc, skip);
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
 
     GatherArgs a;

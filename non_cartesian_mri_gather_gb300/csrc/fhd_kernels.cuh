@@ -82,9 +82,10 @@ constexpr int kTile = FHD_TILE;          // sources per staged tile
 constexpr int kStages = FHD_STAGES;      // shared-memory ring depth
 constexpr int kRecordBytes = 32;         // one packed source
 constexpr int kTileBytes = kTile * kRecordBytes;
-// Source segments: kSegment consecutive packed sources whose coordinates are
-// exactly equally spaced take the source-side recurrence; one 16-byte
-// descriptor {step.x, step.y, step.z, flag} per segment, kDescBytes per tile.
+// Source segments: kSegment consecutive packed sources (fast mode; accurate
+// mode's length is set below) whose coordinates are exactly equally spaced
+// take the source-side recurrence; one 16-byte descriptor {step.x, step.y,
+// step.z, flag} per segment, at most kDescBytes per tile.
 constexpr int kSegment = 16;
 constexpr int kSegmentsPerTile = kTile / kSegment;
 constexpr int kDescBytes = kSegmentsPerTile * 16;
@@ -100,6 +101,21 @@ constexpr uint32_t kStatusProducerTimeout = 2u;
 constexpr uint32_t kStatusDrainTimeout = 4u;
 
 enum Mode : int { kAccurate = 0, kFast = 1 };
+// Source segments are kSegment sources long in fast mode and
+// kSegmentAccurate in accurate mode, where the longer segment halves the
+// per-(target, segment) sincospif cost of the source-side recurrence (its
+// three-term error bound, eps * s^2 / 2, stays below 3e-5 over 32 sources);
+// the descriptor array is sized for kSegment.
+constexpr int kSegmentAccurate = 32;
+static_assert(kTile % kSegmentAccurate == 0, "tiles hold whole segments");
+template <int MODE>
+__host__ __device__ constexpr int segment_len() {
+    return MODE == kAccurate ? kSegmentAccurate : kSegment;
+}
+template <int MODE>
+__host__ __device__ constexpr int segments_per_tile() {
+    return kTile / segment_len<MODE>();
+}
 // The pair-by-pair path walks a thread's kV targets in groups (coordinates and
 // per-tile sums of one group in registers at a time): wider in fast mode,
 // where more independent MUFU operations per warp hide their latency, than in
@@ -170,7 +186,7 @@ struct GatherArgs {
     const float* __restrict__ ty;
     const float* __restrict__ tz;
     const float4* __restrict__ packed;  // n_tiles * kTile records of 2 float4
-    const float4* __restrict__ desc;    // n_tiles * kSegmentsPerTile segment descriptors
+    const float4* __restrict__ desc;    // n_tiles * segments_per_tile<MODE>() segment descriptors
     float* __restrict__ out_r;
     float* __restrict__ out_i;
     float* __restrict__ partial;    // [2*ctas slots][2][kTargetsPerBlock]
@@ -321,7 +337,7 @@ __global__ void pack_sources(const float* __restrict__ ax, const float* __restri
     }
 }
 
-// Segment descriptors: one thread per kSegment sources.  A segment is flagged
+// Segment descriptors: one thread per SEG sources.  A segment is flagged
 // when its real sources (index < n) have coordinates a_s = a_0 + (s - s0) * D
 // exactly (checked in double on the caller's unscaled coordinates, where these
 // products and sums are exact); the descriptor holds the scaled step
@@ -329,14 +345,15 @@ __global__ void pack_sources(const float* __restrict__ ax, const float* __restri
 // fl(scale * a_s), so A_0 + s * fl(scale * D) differs from them only by
 // rounding (fast mode's scale 2 pi breaks exact spacing of the packed values
 // themselves).  Sources at index >= n are zero-weight padding.
+template <int SEG>
 __global__ void describe_segments(const float* __restrict__ ax, const float* __restrict__ ay,
                                   const float* __restrict__ az, float scale, int64_t n, int64_t n_segments,
                                   float4* __restrict__ desc, const uint32_t* skip) {
     if (skip != nullptr && *skip != 0u) return;
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < n_segments;
          g += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t s0 = g * kSegment;
-        const int64_t real = n - s0 < kSegment ? (n - s0 > 0 ? n - s0 : 0) : kSegment;
+        const int64_t s0 = g * SEG;
+        const int64_t real = n - s0 < SEG ? (n - s0 > 0 ? n - s0 : 0) : SEG;
         float4 out = make_float4(0.f, 0.f, 0.f, 1.f);
         if (real >= 2) {
             const double x0 = ax[s0], y0 = ay[s0], z0 = az[s0];
@@ -622,6 +639,7 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
                                                             const float4* __restrict__ desc,
                                                             const float (*coord)[kThreads], float (*run)[kThreads],
                                                             int tid) {
+    constexpr int kSeg = segment_len<MODE>();
 #pragma unroll 1
     for (int g = 0; g < kV; g += kSourceGroup) {
         float bx[kSourceGroup], by[kSourceGroup], bz[kSourceGroup];
@@ -639,9 +657,9 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
         float cu[kSourceGroup], su[kSourceGroup];
         float4 d_prev = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-        for (int j = 0; j < kSegmentsPerTile; ++j) {
-            const float4 b0 = rec[2 * j * kSegment];      // A_0.x A_0.x A_0.y A_0.y
-            const float4 b1 = rec[2 * j * kSegment + 1];  // A_0.z A_0.z w.re w.im
+        for (int j = 0; j < segments_per_tile<MODE>(); ++j) {
+            const float4 b0 = rec[2 * j * kSeg];      // A_0.x A_0.x A_0.y A_0.y
+            const float4 b1 = rec[2 * j * kSeg + 1];  // A_0.z A_0.z w.re w.im
             const float4 d = desc[j];
             if (j == 0 || d.x != d_prev.x || d.y != d_prev.y || d.z != d_prev.z) {  // uniform over the CTA
 #pragma unroll
@@ -678,15 +696,15 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
                 }
             }
 #pragma unroll
-            for (int s = 1; s < kSegment; ++s) {
-                const float4 w = rec[2 * (j * kSegment + s) + 1];  // w.re, w.im in .z, .w
+            for (int s = 1; s < kSeg; ++s) {
+                const float4 w = rec[2 * (j * kSeg + s) + 1];  // w.re, w.im in .z, .w
                 const float sg = strided_negated(s) ? -1.f : 1.f;   // s_s, folded into the weight
                 const f2_t wr = f2_pack(sg * w.z, sg * w.z), wi = f2_pack(sg * w.w, sg * w.w);
 #pragma unroll
                 for (int v = 0; v < kSourceGroup; ++v) {
                     P[v] = f2_fma(wr, f[v], P[v]);
                     Q[v] = f2_fma(wi, f[v], Q[v]);
-                    if (s + 1 < kSegment) {
+                    if (s + 1 < kSeg) {
                         const f2_t fn = f2_fma((s & 1) ? kneg[v] : kpos[v], f[v], fm[v]);  // f_{s+1}
                         fm[v] = f[v];
                         f[v] = fn;
@@ -766,9 +784,10 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
             }
             if (w == args.skip_tile) continue;  // test hook: this copy never arrives
             const int64_t j = w % sch.n_tiles;
-            mbar_arrive_expect_tx(&sm.full[st], kTileBytes + kDescBytes);
+            constexpr int kTileDescBytes = segments_per_tile<MODE>() * 16;
+            mbar_arrive_expect_tx(&sm.full[st], kTileBytes + kTileDescBytes);
             bulk_copy_g2s(&sm.ring[st][0], args.packed + j * (kTile * 2), kTileBytes, &sm.full[st]);
-            bulk_copy_g2s(&sm.desc[st][0], args.desc + j * kSegmentsPerTile, kDescBytes, &sm.full[st]);
+            bulk_copy_g2s(&sm.desc[st][0], args.desc + j * segments_per_tile<MODE>(), kTileDescBytes, &sm.full[st]);
         }
         // Drain: the last copy issued into each stage must have landed before
         // this CTA's shared memory can be released.
@@ -866,7 +885,8 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
         } else {
             bool src_strided = args.allow_strided != 0;
 #pragma unroll
-            for (int q = 0; q < kSegmentsPerTile; ++q) src_strided = src_strided && sm.desc[st][q].w != 0.f;
+            for (int q = 0; q < segments_per_tile<MODE>(); ++q)
+                src_strided = src_strided && sm.desc[st][q].w != 0.f;
             if (src_strided) {
                 if constexpr (MODE == kFast)
                     accumulate_tile_src_strided<MODE>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);

@@ -329,14 +329,15 @@ def test_fhd_spoke_sources_random_voxels(mode):
 
 @pytest.mark.parametrize("mode", ALL_MODES)
 def test_source_recurrence_step_changes_within_tile(mode):
-    """Spokes of 48 samples (three 16-source segments each): every 256-source
-    tile holds segments of several spokes, so the segment step changes inside
-    a tile and the step phasor is re-evaluated there."""
-    k = _spokes(23, 12, points=48)
+    """Spokes of 96 samples (six 16-source segments in fast mode, three
+    32-source segments in accurate mode): every 256-source tile holds
+    segments of several spokes, so the segment step changes inside a tile
+    and the step phasor is re-evaluated there."""
+    k = _spokes(23, 12, points=96)
     p = random_problem(4000, k.shape[0], kmax=1.0, seed=12)
     p.kx, p.ky, p.kz = (np.ascontiguousarray(k[:, i]) for i in range(3))
     ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
-    check(gpu_fhd(p, mode), ref, mode, "F^H D 48-sample spoke sources")
+    check(gpu_fhd(p, mode), ref, mode, "F^H D 96-sample spoke sources")
 
 
 # ------------------------------------------------------------ edge cases
