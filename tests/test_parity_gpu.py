@@ -275,13 +275,16 @@ def _spokes(n_spokes, seed, points=256):
 
 @pytest.mark.parametrize("side", [32, 24])
 @pytest.mark.parametrize("mode", ALL_MODES)
-def test_fwd_grid_voxel_sources(side, mode):
+@pytest.mark.parametrize("drop", [0, 5])
+def test_fwd_grid_voxel_sources(side, mode, drop):
     """F rho with the voxels of a side^3 grid as sources: rows of 32 split into
-    equally spaced 16-source segments (source recurrence); rows of 24 make
-    segments straddle rows, so those tiles are evaluated pair by pair."""
+    equally spaced segments of 16 (fast mode) or 32 (accurate mode) sources
+    (source recurrence); rows of 24 make segments straddle rows, so those
+    tiles are evaluated pair by pair.  drop = 5 leaves the last segment with
+    fewer real sources than its length (the rest zero-weight padding)."""
     from inputs import grid_coords
 
-    x, y, z = grid_coords(side, side, side)
+    x, y, z = (a[: a.size - drop] for a in grid_coords(side, side, side))
     p = random_problem(x.size, 1500, kmax=side / 2, seed=side, op="fwd")
     p.x, p.y, p.z = x, y, z
     ref = oracle.forward(p.x, p.y, p.z, p.rho_r + 1j * p.rho_i, p.kx, p.ky, p.kz)
