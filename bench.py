@@ -75,15 +75,16 @@ def per_pair_counts(path: str):
         g = 16.0
         return 7.0 + 13.0 / g, 2.0 * (g - 1) / g, 9.0 - 2.0 / g + 13.0 / g
     if path == "source":
-        # source-side recurrence, segments of S = 16 sources, groups of G = 8
-        # targets, packed f32x2: per pair one packed three-term step and two
-        # packed FMAs into P = sum w.re e and Q = sum w.im e (6 lane
+        # source-side recurrence (the forward gather: segments of S = 32
+        # voxel sources), groups of G = 8 targets, packed f32x2: per pair one
+        # packed three-term step and two packed FMAs into P = sum w.re e and
+        # Q = sum w.im e (6 lane
         # operations, 3 instructions); per (target, segment) the phase of e_0
         # (3), e_1 = e_0 u (4), 2 cos (1), the signed pair of 2 cos (2) and
         # 2 MUFU (the step phasor u once per run of segments with the same
         # step: once per tile on an image grid, not counted); per (source,
         # group) one shared-memory load and the two signed weight pairs (4).
-        S, G = 16.0, 8.0
+        S, G = 32.0, 8.0
         return 6.0 + 10.0 / S, 2.0 / S, 3.0 + 12.0 / S + 5.0 / G
     # recurrence, V targets per thread.  Per (thread, sample): the two phases
     # as 3 packed instructions (6 lane operations), g_0 = D exp(i theta_0) (4),

@@ -28,9 +28,11 @@ cudaError_t max_ctas(int device, fhd_mode mode, int* out) {
     int per_sm = 0;
     const size_t smem = sizeof(GatherSmem);
     if (fast_mode(mode))
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<kFast, kFastPolySlots>, kCtaThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, gather_kernel<kFast, kFastPolySlots, segment_len<kFast>()>, kCtaThreads, smem);
     else
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<kAccurate, 0>, kCtaThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, gather_kernel<kAccurate, 0, segment_len<kAccurate>()>, kCtaThreads, smem);
     if (e != cudaSuccess) return e;
     per_sm = std::min(std::max(per_sm, 1), kMinCtasPerSm);
     *out = sms * per_sm;
@@ -190,14 +192,17 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     }
 
     float4* desc = reinterpret_cast<float4*>(ws + L.desc);
-    const int64_t n_segments = padded / (fast_mode(mode) ? segment_len<kFast>() : segment_len<kAccurate>());
+    // The forward gather (voxel sources, sign -1) and accurate mode use
+    // kSegmentAccurate-source segments, the fast adjoint gather kSegment.
+    const bool long_segments = g.sign < 0.f || !fast_mode(mode);
+    const int64_t n_segments = padded / (long_segments ? kSegmentAccurate : kSegment);
     const int desc_grid = (int)std::min<int64_t>(ceil_div(n_segments, 256), (int64_t)sms * 8);
-    if (fast_mode(mode))
-        describe_segments<segment_len<kFast>()><<<desc_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, scale, g.n_sources,
-                                                                                 n_segments, desc, skip);
+    if (long_segments)
+        describe_segments<kSegmentAccurate><<<desc_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, scale, g.n_sources,
+                                                                           n_segments, desc, skip);
     else
-        describe_segments<segment_len<kAccurate>()><<<desc_grid, 256, 0, stream>>>(
-            g.sx, g.sy, g.sz, scale, g.n_sources, n_segments, desc, skip);
+        describe_segments<kSegment><<<desc_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, scale, g.n_sources, n_segments,
+                                                                   desc, skip);
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
 
     GatherArgs a;
@@ -219,11 +224,19 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     if (ev_start && (e = cudaEventRecord(ev_start, stream)) != cudaSuccess) return FHD_ERR_CUDA;
     const size_t smem = sizeof(GatherSmem);
     if (fast_mode(mode)) {
-        cudaFuncSetAttribute(gather_kernel<kFast, kFastPolySlots>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        gather_kernel<kFast, kFastPolySlots><<<sch.ctas, kCtaThreads, smem, stream>>>(a);
+        if (g.sign < 0.f) {
+            constexpr auto k = gather_kernel<kFast, kFastPolySlots, kSegmentAccurate>;
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            k<<<sch.ctas, kCtaThreads, smem, stream>>>(a);
+        } else {
+            constexpr auto k = gather_kernel<kFast, kFastPolySlots, kSegment>;
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            k<<<sch.ctas, kCtaThreads, smem, stream>>>(a);
+        }
     } else {
-        cudaFuncSetAttribute(gather_kernel<kAccurate, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        gather_kernel<kAccurate, 0><<<sch.ctas, kCtaThreads, smem, stream>>>(a);
+        constexpr auto k = gather_kernel<kAccurate, 0, kSegmentAccurate>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<sch.ctas, kCtaThreads, smem, stream>>>(a);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
     if (sch.ctas > 1) {

@@ -108,13 +108,12 @@ enum Mode : int { kAccurate = 0, kFast = 1 };
 // the descriptor array is sized for kSegment.
 constexpr int kSegmentAccurate = 32;
 static_assert(kTile % kSegmentAccurate == 0, "tiles hold whole segments");
+// Segment length of the adjoint gather in each mode; the forward gather
+// (voxel sources) takes kSegmentAccurate in both modes, in a kernel
+// instantiation of its own.
 template <int MODE>
 __host__ __device__ constexpr int segment_len() {
     return MODE == kAccurate ? kSegmentAccurate : kSegment;
-}
-template <int MODE>
-__host__ __device__ constexpr int segments_per_tile() {
-    return kTile / segment_len<MODE>();
 }
 // The pair-by-pair path walks a thread's kV targets in groups (coordinates and
 // per-tile sums of one group in registers at a time): wider in fast mode,
@@ -186,7 +185,7 @@ struct GatherArgs {
     const float* __restrict__ ty;
     const float* __restrict__ tz;
     const float4* __restrict__ packed;  // n_tiles * kTile records of 2 float4
-    const float4* __restrict__ desc;    // n_tiles * segments_per_tile<MODE>() segment descriptors
+    const float4* __restrict__ desc;    // n_tiles * (kTile / SEG) segment descriptors
     float* __restrict__ out_r;
     float* __restrict__ out_i;
     float* __restrict__ partial;    // [2*ctas slots][2][kTargetsPerBlock]
@@ -634,12 +633,12 @@ __device__ __forceinline__ bool equally_spaced(const float (&c)[kV], int n, floa
 // sum w_s e_s = (P.re - Q.im) + i (P.im + Q.re) at the end: per pair three
 // packed FMAs.  Targets go in groups of kSourceGroup; each group's tile sums
 // are folded straight into the thread's running sums.
-template <int MODE>
+template <int MODE, int SEG>
 __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __restrict__ rec,
                                                             const float4* __restrict__ desc,
                                                             const float (*coord)[kThreads], float (*run)[kThreads],
                                                             int tid) {
-    constexpr int kSeg = segment_len<MODE>();
+    constexpr int kSeg = SEG;
 #pragma unroll 1
     for (int g = 0; g < kV; g += kSourceGroup) {
         float bx[kSourceGroup], by[kSourceGroup], bz[kSourceGroup];
@@ -657,7 +656,7 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
         float cu[kSourceGroup], su[kSourceGroup];
         float4 d_prev = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-        for (int j = 0; j < segments_per_tile<MODE>(); ++j) {
+        for (int j = 0; j < kTile / kSeg; ++j) {
             const float4 b0 = rec[2 * j * kSeg];      // A_0.x A_0.x A_0.y A_0.y
             const float4 b1 = rec[2 * j * kSeg + 1];  // A_0.z A_0.z w.re w.im
             const float4 d = desc[j];
@@ -734,18 +733,20 @@ __device__ __noinline__ void accumulate_tile_ool(const float4* __restrict__ rec,
                                                  float (*run)[kThreads], int tid) {
     accumulate_tile<MODE, NPOLY>(rec, coord, run, tid);
 }
-template <int MODE>
+template <int MODE, int SEG>
 __device__ __noinline__ void accumulate_tile_src_strided_ool(const float4* __restrict__ rec,
                                                              const float4* __restrict__ desc,
                                                              const float (*coord)[kThreads],
                                                              float (*run)[kThreads], int tid) {
-    accumulate_tile_src_strided<MODE>(rec, desc, coord, run, tid);
+    accumulate_tile_src_strided<MODE, SEG>(rec, desc, coord, run, tid);
 }
 
 // MODE: kAccurate or kFast.  NPOLY (fast mode only): how many of the kV
 // register slots evaluate sin/cos with the FMA-pipe polynomial instead of the
-// MUFU pipe; it sets the split between the two pipes.
-template <int MODE, int NPOLY>
+// MUFU pipe; it sets the split between the two pipes.  SEG: the source segment
+// length of the descriptors (segment_len<MODE>() for the adjoint gather,
+// kSegmentAccurate for the forward gather, each its own instantiation).
+template <int MODE, int NPOLY, int SEG>
 __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(const GatherArgs args) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     GatherSmem& sm = *reinterpret_cast<GatherSmem*>(smem_raw);
@@ -784,10 +785,10 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
             }
             if (w == args.skip_tile) continue;  // test hook: this copy never arrives
             const int64_t j = w % sch.n_tiles;
-            constexpr int kTileDescBytes = segments_per_tile<MODE>() * 16;
+            constexpr int kTileDescBytes = kTile / SEG * 16;
             mbar_arrive_expect_tx(&sm.full[st], kTileBytes + kTileDescBytes);
             bulk_copy_g2s(&sm.ring[st][0], args.packed + j * (kTile * 2), kTileBytes, &sm.full[st]);
-            bulk_copy_g2s(&sm.desc[st][0], args.desc + j * segments_per_tile<MODE>(), kTileDescBytes, &sm.full[st]);
+            bulk_copy_g2s(&sm.desc[st][0], args.desc + j * (kTile / SEG), kTileDescBytes, &sm.full[st]);
         }
         // Drain: the last copy issued into each stage must have landed before
         // this CTA's shared memory can be released.
@@ -885,13 +886,13 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
         } else {
             bool src_strided = args.allow_strided != 0;
 #pragma unroll
-            for (int q = 0; q < segments_per_tile<MODE>(); ++q)
+            for (int q = 0; q < kTile / SEG; ++q)
                 src_strided = src_strided && sm.desc[st][q].w != 0.f;
             if (src_strided) {
                 if constexpr (MODE == kFast)
-                    accumulate_tile_src_strided<MODE>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
+                    accumulate_tile_src_strided<MODE, SEG>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
                 else
-                    accumulate_tile_src_strided_ool<MODE>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
+                    accumulate_tile_src_strided_ool<MODE, SEG>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
             } else {
                 if constexpr (MODE == kFast)
                     accumulate_tile<MODE, NPOLY>(rec, sm.coord, sm.run, tid);
