@@ -79,3 +79,38 @@ def test_fhd_past_2_pow_31_voxels(big, mode):
     ref = oracle.adjoint(kx, ky, kz, Dr + 1j * Di, *grid_coords_at(idx, NX, NY, NZ))
     err = rel_l2(got, ref)
     assert err <= (TOL_ACCURATE if mode == 0 else TOL_FAST), f"relL2 {err:.3e} (mode {mode})"
+
+
+# ------------------------------------------------------------ many samples
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_split_gather_four_million_samples(mode):
+    """256 voxels x 2^22 samples: the split gather with 1216 slices of the
+    sample range (the most it uses) against the oracle on every voxel."""
+    import non_cartesian_mri_gather_gb300 as fhd
+    from inputs import random_problem
+    from tests.gpu_helpers import gpu_fhd
+
+    lib = fhd.load()
+    p = random_problem(256, 1 << 22, kmax=24.0, seed=42)
+    assert lib.fhd_test_split_shape(p.N, p.M, 152, 152, 2 * 152 * 2 * 8192 * 4, None, None) == 1
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    err = rel_l2(gpu_fhd(p, mode), ref)
+    assert err <= (TOL_ACCURATE if mode == 0 else TOL_FAST), f"relL2 {err:.3e}"
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_persistent_gather_million_samples(mode):
+    """A 64 x 64 x 16 voxel grid x 2^20 samples: 8 target blocks x 4096 sample
+    tiles on the persistent gather (every CTA's range splits blocks), checked
+    on 512 sampled voxels, first and last included."""
+    from inputs import grid_coords, random_problem
+    from tests.gpu_helpers import gpu_fhd, sample_indices
+
+    p = random_problem(65536, 1 << 20, kmax=24.0, seed=43)
+    p.x, p.y, p.z = grid_coords(64, 64, 16)
+    got = gpu_fhd(p, mode)
+    idx = np.unique(np.concatenate([[0, p.N - 1], sample_indices(p.N, 512)]))
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x[idx], p.y[idx], p.z[idx])
+    err = rel_l2(got[idx], ref)
+    assert err <= (TOL_ACCURATE if mode == 0 else TOL_FAST), f"relL2 {err:.3e}"
