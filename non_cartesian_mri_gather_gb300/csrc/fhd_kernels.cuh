@@ -93,6 +93,7 @@ static_assert(kTile % kSegment == 0, "tiles hold whole segments");
 constexpr int kCtaThreads = kThreads + 32;  // + one producer warp
 constexpr int kMinCtasPerSm = FHD_MIN_CTAS_PER_SM;
 constexpr int kUnroll = FHD_UNROLL;      // sources per unrolled inner-loop step
+constexpr int kUnrollSharedU = 8;        // the same in the accurate warp-shared-phasor loop (measured best)
 static_assert(kThreads % 32 == 0 && kTile % 2 == 0 && kStages >= 2, "bad launch shape");
 
 // status word bits
@@ -546,7 +547,7 @@ __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* _
             const float4 r1 = rec[2 * (s32 + lane) + 1];
             phasor_accurate(fmaf(r1.y, dz, fmaf(r0.w, dy, r0.y * dx)), su_l, cu_l);
         }
-#pragma unroll kUnroll
+#pragma unroll kUnrollSharedU
         for (int q = 0; q < 32; ++q) {
             const float4 r0 = rec[2 * (s32 + q)];      // A.x A.x A.y A.y
             const float4 r1 = rec[2 * (s32 + q) + 1];  // A.z A.z w.re w.im
