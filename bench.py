@@ -355,7 +355,7 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------- GPU arm
 def gather_launches(fhd, shape, sms, n_targets, n_sources):
     """Kernels one gather of the library launches: pack, describe, gather and
-    fix-up on the persistent path (no fix-up with a single CTA); pack, split
+    fix-up on the persistent path (no fix-up with a single CTA); the split
     gather and (with more than one slice) the slice reduction on the split
     path, which the library takes by the rule fhd_test_split_shape reports."""
     import ctypes
@@ -366,7 +366,7 @@ def gather_launches(fhd, shape, sms, n_targets, n_sources):
     split = fhd.load().fhd_test_split_shape(n_targets, n_sources, sms, shape["ctas"], partial_bytes,
                                             ctypes.byref(k), None)
     if split == 1:
-        return 2 + (1 if k.value > 1 else 0)
+        return 1 + (1 if k.value > 1 else 0)
     work = -(-n_targets // per_block) * -(-n_sources // shape["tile_sources"])
     return 3 + (1 if min(work, shape["ctas"]) > 1 else 0)
 

@@ -160,11 +160,7 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     const int64_t padded = sch.n_tiles * kTile;
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    const int pack_grid = (int)std::min<int64_t>(ceil_div(padded, 256), (int64_t)sms * 8);
     const float scale = g.sign * (fast_mode(mode) ? 6.28318530717958647692f : 1.0f);
-    pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, scale, g.n_sources, padded,
-                                                packed, status, first_pass ? 1 : 0, skip);
-    if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
 
     const SplitShape split = split_shape(g.n_targets, g.n_sources, sms, ctas_max, L.frho - L.partial);
     bool use_split = split.worth_it;
@@ -173,14 +169,17 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     if (forced == 2) use_split = true;
     if (skip_tile >= 0) use_split = false;  // the skipped tile belongs to the persistent schedule
     if (use_split) {
+        // reads the caller's source arrays itself: no pack kernel
         if (ev_start && (e = cudaEventRecord(ev_start, stream)) != cudaSuccess) return FHD_ERR_CUDA;
         const dim3 grid((unsigned)ceil_div(g.n_targets, kSplitThreads), (unsigned)split.n_slices);
         if (fast_mode(mode))
             split_gather_kernel<kFast><<<grid, kSplitThreads, 0, stream>>>(
-                g.tx, g.ty, g.tz, g.n_targets, packed, g.n_sources, split.slice_len, partial, g.out_r, g.out_i, skip);
+                g.tx, g.ty, g.tz, g.n_targets, g.sx, g.sy, g.sz, g.wr, g.wi, scale, g.n_sources, split.slice_len,
+                partial, g.out_r, g.out_i, status, first_pass ? 1 : 0, skip);
         else
             split_gather_kernel<kAccurate><<<grid, kSplitThreads, 0, stream>>>(
-                g.tx, g.ty, g.tz, g.n_targets, packed, g.n_sources, split.slice_len, partial, g.out_r, g.out_i, skip);
+                g.tx, g.ty, g.tz, g.n_targets, g.sx, g.sy, g.sz, g.wr, g.wi, scale, g.n_sources, split.slice_len,
+                partial, g.out_r, g.out_i, status, first_pass ? 1 : 0, skip);
         if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
         if (split.n_slices > 1) {
             split_reduce_kernel<<<(unsigned)ceil_div(g.n_targets, 32), 32 * kReduceWarps, 0, stream>>>(
@@ -190,6 +189,11 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
         if (ev_stop && (e = cudaEventRecord(ev_stop, stream)) != cudaSuccess) return FHD_ERR_CUDA;
         return FHD_OK;
     }
+
+    const int pack_grid = (int)std::min<int64_t>(ceil_div(padded, 256), (int64_t)sms * 8);
+    pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, scale, g.n_sources, padded,
+                                                packed, status, first_pass ? 1 : 0, skip);
+    if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
 
     float4* desc = reinterpret_cast<float4*>(ws + L.desc);
     // The forward gather (voxel sources, sign -1) and accurate mode use

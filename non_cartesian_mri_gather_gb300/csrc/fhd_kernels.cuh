@@ -977,7 +977,8 @@ __global__ void __launch_bounds__(kFixupThreads) fixup_kernel(const Schedule sch
 // source tiles, so most CTAs or most threads would idle) take this path: one
 // target per thread, kSplitThreads targets per CTA along x, the sources split
 // into n_slices equal slices along y.  Each CTA stages its slice through
-// shared memory kSplitChunk records at a time and evaluates every pair
+// shared memory kSplitChunk sources at a time, read straight from the
+// caller's arrays (no pack kernel on this path), and evaluates every pair
 // directly (one phasor per pair, as on the pair-by-pair path); a slice's sums
 // go to its own partial row, and split_reduce_kernel adds the rows in a fixed
 // order (no atomics, bit-reproducible).  With one slice the CTA writes the
@@ -988,10 +989,16 @@ constexpr int kSplitChunk = 256;
 template <int MODE>
 __global__ void __launch_bounds__(kSplitThreads) split_gather_kernel(
     const float* __restrict__ tx, const float* __restrict__ ty, const float* __restrict__ tz, int64_t n_targets,
-    const float4* __restrict__ packed, int64_t n_sources, int64_t slice_len, float* __restrict__ partial,
-    float* __restrict__ out_r, float* __restrict__ out_i, const uint32_t* skip) {
+    const float* __restrict__ ax, const float* __restrict__ ay, const float* __restrict__ az,
+    const float* __restrict__ wr, const float* __restrict__ wi, float scale, int64_t n_sources, int64_t slice_len,
+    float* __restrict__ partial, float* __restrict__ out_r, float* __restrict__ out_i, uint32_t* status,
+    int reset_status, const uint32_t* skip) {
     if (skip != nullptr && *skip != 0u) return;
-    __shared__ float4 rec[2 * kSplitChunk];
+    if (reset_status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0u;
+    // a chunk of sources as (A.x, A.y, A.z) with A = scale * a, rounded once
+    // as pack_sources rounds them, and their weights
+    __shared__ float4 rec[kSplitChunk];
+    __shared__ float2 wrec[kSplitChunk];
     const int64_t t = (int64_t)blockIdx.x * kSplitThreads + threadIdx.x;
     const bool active = t < n_targets;
     const float bx = active ? tx[t] : 0.f, by = active ? ty[t] : 0.f, bz = active ? tz[t] : 0.f;
@@ -1001,22 +1008,26 @@ __global__ void __launch_bounds__(kSplitThreads) split_gather_kernel(
     for (int64_t c0 = s0; c0 < s1; c0 += kSplitChunk) {
         const int n = (int)(s1 - c0 < kSplitChunk ? s1 - c0 : kSplitChunk);
         __syncthreads();  // the previous chunk is consumed
-        for (int i = threadIdx.x; i < 2 * n; i += kSplitThreads) rec[i] = packed[2 * c0 + i];
+        for (int i = threadIdx.x; i < n; i += kSplitThreads) {
+            const int64_t q = c0 + i;
+            rec[i] = make_float4(scale * ax[q], scale * ay[q], scale * az[q], 0.f);
+            wrec[i] = make_float2(wr[q], wi[q]);
+        }
         __syncthreads();
 #pragma unroll 4
         for (int s = 0; s < n; ++s) {
-            const float4 r0 = rec[2 * s];      // A.x A.x A.y A.y
-            const float4 r1 = rec[2 * s + 1];  // A.z A.z w.re w.im
-            const float p = fmaf(r1.x, bz, fmaf(r0.z, by, r0.x * bx));
+            const float4 r = rec[s];
+            const float2 w = wrec[s];
+            const float p = fmaf(r.z, bz, fmaf(r.y, by, r.x * bx));
             float sn, cs;
             if constexpr (MODE == kAccurate)
                 phasor_accurate(p, sn, cs);
             else
                 phasor_mufu(p, sn, cs);
-            ar = fmaf(r1.z, cs, ar);
-            ar = fmaf(-r1.w, sn, ar);
-            ai = fmaf(r1.z, sn, ai);
-            ai = fmaf(r1.w, cs, ai);
+            ar = fmaf(w.x, cs, ar);
+            ar = fmaf(-w.y, sn, ar);
+            ai = fmaf(w.x, sn, ai);
+            ai = fmaf(w.y, cs, ai);
         }
     }
     if (!active) return;
