@@ -20,14 +20,27 @@ namespace host {
 
 constexpr int kVersion = 100;  // 0.1.0
 
-// Resident CTAs of the gather kernel on `device` (SMs x CTAs per SM).
+// Resident CTAs of the gather kernel on `device` (SMs x CTAs per SM), queried
+// once per (device, mode) and cached: it depends only on the device and the
+// compiled kernel.
+constexpr int kCtaCacheDevices = 64;
+std::atomic<int> g_ctas_cache[kCtaCacheDevices][2];  // 0: not yet queried
+
 cudaError_t max_ctas(int device, fhd_mode mode, int* out) {
+    const int fast = fast_mode(mode) ? 1 : 0;
+    if (device >= 0 && device < kCtaCacheDevices) {
+        const int cached = g_ctas_cache[device][fast].load(std::memory_order_relaxed);
+        if (cached > 0) {
+            *out = cached;
+            return cudaSuccess;
+        }
+    }
     int sms = 0;
     cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     const size_t smem = sizeof(GatherSmem);
-    if (fast_mode(mode))
+    if (fast)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
             &per_sm, gather_kernel<kFast, kFastPolySlots, segment_len<kFast>()>, kCtaThreads, smem);
     else
@@ -36,6 +49,7 @@ cudaError_t max_ctas(int device, fhd_mode mode, int* out) {
     if (e != cudaSuccess) return e;
     per_sm = std::min(std::max(per_sm, 1), kMinCtasPerSm);
     *out = sms * per_sm;
+    if (device >= 0 && device < kCtaCacheDevices) g_ctas_cache[device][fast].store(*out, std::memory_order_relaxed);
     return cudaSuccess;
 }
 
