@@ -29,9 +29,11 @@
  *            256-byte aligned.
  * Ownership  all pointers are owned by the caller and must be device memory
  *            of the current CUDA device (cudaMalloc'd or managed).  The
- *            library allocates no memory, keeps no pointer after a call
- *            returns and holds no global state (the one exception is the
- *            static scratch array of fhd_compute_noalloc, described there).
+ *            library allocates no memory and keeps no pointer after a call
+ *            returns.  Its only process-wide state: a cache of each device's
+ *            resident gather CTA count (filled on first use), the static
+ *            scratch array of fhd_compute_noalloc (described there) and the
+ *            path setting of the test hook fhd_test_set_path.
  * Outputs    are overwritten, never accumulated into.  Outputs must not
  *            overlap any input, each other, or the workspace.
  * Async      a call validates its arguments on the host, enqueues its kernels
