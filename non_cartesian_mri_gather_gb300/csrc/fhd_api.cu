@@ -472,8 +472,9 @@ int fhd_version(void) { return kVersion; }
 // static device array instead.  Layout inside it is the same layout_for()
 // layout fhd_compute uses, which fits because M and the resident CTA count are
 // capped; everything the kernels read from it is written earlier in the same
-// call (pack_sources clears the status word and rewrites every record; each
-// partial slot the fix-up reads is written by its CTA first).
+// call (pack_sources, or on the small-problem path the split gather, clears
+// the status word; pack_sources rewrites every record; each partial slot or
+// row that a fix-up or reduction reads is written first by its CTA).
 namespace {
 
 // FHD_NOALLOC_SCRATCH_BYTES is the size for the default launch shape (8192

@@ -66,7 +66,9 @@ fhd_status check_array(const void* p, size_t bytes, size_t align, int device);
 fhd_status validate(fhd_op op, int64_t N, int64_t M, fhd_mode mode, const Buf* ins, int n_in, const Buf* outs,
                     int n_out, void* workspace, size_t workspace_bytes, int* device_out, Layout* L);
 
-// Enqueue pack, gather and fix-up for one gather on `stream`.  `skip`, when
+// Enqueue one gather on `stream`: pack, describe, the persistent gather and
+// its fix-up; or, for problems too small to fill the persistent CTAs (see
+// split_shape), the split gather and its slice reduction.  `skip`, when
 // not NULL, is a device word: if it is non-zero when the kernels start they
 // return at once (used to stop a conjugate-gradient loop on the device).
 fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, const Layout& L, int device,

@@ -28,9 +28,16 @@
 //                       record as a broadcast (the role the constant cache
 //                       plays in section 17.3.4), keep per-tile accumulators
 //                       of kV consecutive targets in registers (privatisation,
-//                       section 17.3.3) and write every output once.  Equally
-//                       spaced targets take a recurrence instead of a sin/cos
-//                       per pair (accumulate_tile_strided).
+//                       section 17.3.3) and write every output once.  Per warp
+//                       and tile one of three paths: equally spaced targets
+//                       take a recurrence instead of a sin/cos per pair
+//                       (accumulate_tile_strided); otherwise tiles of equally
+//                       spaced source segments (described by
+//                       describe_segments) a source-side recurrence
+//                       (accumulate_tile_src_strided); otherwise pair by pair
+//                       (accumulate_tile).  Instantiated per mode and source
+//                       segment length: the fast adjoint gather, the fast
+//                       forward gather and the accurate gather.
 //   3. fixup_kernel   - target blocks whose source range was split between
 //                       CTAs are summed from per-CTA partials in a fixed
 //                       order (no atomics, bit-reproducible).
