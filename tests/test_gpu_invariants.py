@@ -177,3 +177,48 @@ def test_timeout_is_reported_and_context_survives():
 
     ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
     assert rel_l2(host_complex(*out), ref) <= TOL_ACCURATE
+
+
+# ------------------------------------------------------------ profiling entry point and launch shape
+
+@pytest.mark.parametrize("N,M", [(1024, 2048), (65536, 4096)])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_profiled_call_matches_and_times_the_gather(N, M, mode):
+    """fhd_compute_profiled gives fhd_compute's result bit for bit (split path
+    for the small size, persistent gather for the large one) and its two
+    events bracket a positive device time shorter than the whole call's."""
+    import torch
+
+    import non_cartesian_mri_gather_gb300 as fhd
+    from inputs import random_problem
+
+    p = random_problem(N, M, kmax=16.0, seed=N + M)
+    t = {k: dev(getattr(p, k)) for k in ("kx", "ky", "kz", "Dr", "Di", "x", "y", "z")}
+    ws = fhd.Workspace(fhd.OP_FHD, N, M)
+    args = [t[k] for k in ("kx", "ky", "kz", "Dr", "Di", "x", "y", "z")]
+    a = fhd.fhd_compute(*args, mode=mode, workspace=ws)
+    out = (torch.empty(N, device="cuda"), torch.empty(N, device="cuda"))
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record()
+    fhd.fhd_compute_profiled(*args, out[0], out[1], mode, ws, g0, g1)
+    c1.record()
+    torch.cuda.synchronize()
+    assert np.array_equal(host_complex(*a), host_complex(*out))
+    gather_ms, call_ms = g0.elapsed_time(g1), c0.elapsed_time(c1)
+    assert 0.0 < gather_ms <= call_ms
+
+
+def test_launch_shape():
+    import torch
+
+    import non_cartesian_mri_gather_gb300 as fhd
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for mode in (0, 1, 2, 3):
+        shape = fhd.fhd_launch_shape(0, mode)
+        assert shape["ctas"] == sms
+        assert (shape["threads"], shape["targets_per_thread"], shape["tile_sources"], shape["stages"]) == (256, 32, 256, 6)
+    lib = fhd.load()
+    vals = [ctypes.c_int(0) for _ in range(5)]
+    assert lib.fhd_launch_shape(0, 4, *(ctypes.addressof(v) for v in vals)) == 1  # unknown mode bit
