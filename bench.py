@@ -518,10 +518,31 @@ def run_ours(args, world, rank, local):
         run_e2e(k2, s2, t2)
         torch.cuda.synchronize()
         ms_e2e = max_over_ranks(s2.elapsed_time(t2) / k2, world)
+
+        # the same steps with the copies in line (one stream, no overlap)
+        def serial_step():
+            for k in names:
+                d[k].copy_(pin[k], non_blocking=True)
+            step()
+            out_r.copy_(rho_r, non_blocking=True)
+            out_i.copy_(rho_i, non_blocking=True)
+
+        serial_step()
+        barrier(world)
+        torch.cuda.synchronize()
+        s3, t3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s3.record(stream)
+        for _ in range(k2):
+            serial_step()
+        t3.record(stream)
+        torch.cuda.synchronize()
+        ms_serial = max_over_ranks(s3.elapsed_time(t3) / k2, world)
         e2e = {"value": world * pairs / (ms_e2e * 1e-3), "unit": "pairs/s", "h2d_bytes_per_step": input_bytes,
                "d2h_bytes_per_step": 2 * p.N * 4, "ms_per_step": ms_e2e, "steps": k2,
                "pipeline": "inputs of step k+1 copied in and the result of step k copied out while step k "
-                           "computes (two copy streams, double-buffered device arrays)"}
+                           "computes (two copy streams, double-buffered device arrays)",
+               "serial": {"value": world * pairs / (ms_serial * 1e-3), "ms_per_step": ms_serial,
+                          "note": "copy in, compute, copy out on one stream, no overlap"}}
 
     if rank != 0:
         return
