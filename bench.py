@@ -137,9 +137,16 @@ def dist_init():
         import torch
         import torch.distributed as dist
 
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        dist.init_process_group(backend=backend)
+        if torch.cuda.is_available():
+            # one rank per GPU: bind the rank to its device before NCCL starts
+            torch.cuda.set_device(local)
+            try:
+                dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+            except TypeError:  # a PyTorch without the device_id argument
+                dist.init_process_group(backend="nccl")
+        else:
+            dist.init_process_group(backend="gloo")
     return world, rank, local
 
 
