@@ -222,3 +222,41 @@ def test_launch_shape():
     lib = fhd.load()
     vals = [ctypes.c_int(0) for _ in range(5)]
     assert lib.fhd_launch_shape(0, 4, *(ctypes.addressof(v) for v in vals)) == 1  # unknown mode bit
+
+
+def test_concurrent_calls_on_two_streams():
+    """Two calls in flight at once on different streams, each with its own
+    workspace (the header's rule), give their sequential results bit for bit:
+    a persistent gather and a split gather, and an F^H F rho beside an F^H D."""
+    import torch
+
+    import non_cartesian_mri_gather_gb300 as fhd
+    from inputs import random_problem
+
+    big = random_problem(65536, 4096, kmax=16.0, seed=51, coords="grid")
+    small = random_problem(1500, 3000, kmax=16.0, seed=52)
+    fhf = random_problem(20000, 3000, kmax=12.0, seed=53, op="fhf")
+    tb = {k: dev(getattr(big, k)) for k in ("kx", "ky", "kz", "Dr", "Di", "x", "y", "z")}
+    ts = {k: dev(getattr(small, k)) for k in ("kx", "ky", "kz", "Dr", "Di", "x", "y", "z")}
+    tf = {k: dev(getattr(fhf, k)) for k in ("x", "y", "z", "rho_r", "rho_i", "kx", "ky", "kz")}
+    ab = [tb[k] for k in ("kx", "ky", "kz", "Dr", "Di", "x", "y", "z")]
+    as_ = [ts[k] for k in ("kx", "ky", "kz", "Dr", "Di", "x", "y", "z")]
+    af = [tf[k] for k in ("x", "y", "z", "rho_r", "rho_i", "kx", "ky", "kz")]
+    wb = fhd.Workspace(fhd.OP_FHD, big.N, big.M)
+    ws_ = fhd.Workspace(fhd.OP_FHD, small.N, small.M)
+    wf = fhd.Workspace(fhd.OP_FHF, fhf.N, fhf.M)
+    ref_b = host_complex(*fhd.fhd_compute(*ab, mode=1, workspace=wb))
+    ref_s = host_complex(*fhd.fhd_compute(*as_, mode=1, workspace=ws_))
+    ref_f = host_complex(*fhd.fhfrho_apply(*af, mode=1, workspace=wf))
+    torch.cuda.synchronize()
+    s1, s2, s3 = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        ob = fhd.fhd_compute(*ab, mode=1, workspace=wb, stream=s1)
+        os_ = fhd.fhd_compute(*as_, mode=1, workspace=ws_, stream=s2)
+        of = fhd.fhfrho_apply(*af, mode=1, workspace=wf, stream=s3)
+        torch.cuda.synchronize()
+        assert np.array_equal(host_complex(*ob), ref_b)
+        assert np.array_equal(host_complex(*os_), ref_s)
+        assert np.array_equal(host_complex(*of), ref_f)
+    for w, s in ((wb, s1), (ws_, s2), (wf, s3)):
+        assert fhd.fhd_workspace_status(w, s) == 0
