@@ -26,10 +26,11 @@ roofline   the gather kernel against its plain-ALU bound
            MUFU pipe for 15 of 16 pairs, an FMA-pipe polynomial for the 16th).
            Equal-spacing recurrence on the benchmark's grid voxels, V = 32 targets per thread, packed f32x2 arithmetic:
            per target one packed add and (from the third target on) one packed
-           three-term step, plus per (thread, sample) the two phases (3 packed
-           instructions), D*exp(i theta_0) (4), its first step (4),
-           2 cos(theta_d) (1) and 4 MUFU -> n_fma = 4 - 4/V + 15/V,
-           n_mufu = 4/V, n_issue = 2 + 14/V.  Maximum SM clock.  The kernel's
+           three-term step (two chains, over even and odd targets), plus per
+           (thread, sample) the two phases (3 packed instructions),
+           D*exp(i theta_0) (4), its first step (4), 2 cos(theta_d) (1),
+           2 cos(2 theta_d) (1) and 4 MUFU -> n_fma = 4 - 4/V + 16/V,
+           n_mufu = 4/V, n_issue = 2 + 15/V.  Maximum SM clock.  The kernel's
            duration comes from CUDA events recorded on its stream around the
            gather and fix-up launches of every timed step.
 cpu_baseline  the fp64 CPU oracle on a bounded voxel sample of the same
@@ -86,15 +87,17 @@ def per_pair_counts(path: str):
         # group) one shared-memory load and the two signed weight pairs (4).
         S, G = 32.0, 8.0
         return 6.0 + 10.0 / S, 2.0 / S, 3.0 + 12.0 / S + 5.0 / G
-    # recurrence, V targets per thread.  Per (thread, sample): the two phases
-    # as 3 packed instructions (6 lane operations), g_0 = D exp(i theta_0) (4),
-    # g_1 = g_0 u (4), 2 cos(theta_d) (1), 4 MUFU.  Per target: one packed add
-    # into its accumulator (2 lane operations), and from the third target on
-    # one packed three-term step (2 lane operations).
+    # recurrence, V targets per thread, as two chains (even and odd targets).
+    # Per (thread, sample): the two phases as 3 packed instructions (6 lane
+    # operations), g_0 = D exp(i theta_0) (4), g_1 = g_0 u (4), 2 cos(theta_d)
+    # (1), 2 cos(2 theta_d) (1), 4 MUFU.  Per target: one packed add into its
+    # accumulator (2 lane operations), and from the third target on one
+    # packed three-term step (2 lane operations; the steps to targets 2 and 3
+    # use 2 cos(theta_d), the rest 2 cos(2 theta_d)).
     V = TARGETS_PER_THREAD
-    lanes = 4.0 - 4.0 / V + 15.0 / V
+    lanes = 4.0 - 4.0 / V + 16.0 / V
     mufu = 4.0 / V
-    issue = (2.0 * V - 2.0 + 3.0 + 4.0 + 4.0 + 1.0 + 4.0) / V
+    issue = (2.0 * V - 2.0 + 3.0 + 4.0 + 4.0 + 1.0 + 1.0 + 4.0) / V
     return lanes, mufu, issue
 
 

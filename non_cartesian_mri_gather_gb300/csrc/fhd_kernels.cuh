@@ -478,6 +478,9 @@ __device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
 
 // Sign of the stored accumulator of target v in the recurrence below.
 __host__ __device__ constexpr bool strided_negated(int v) { return (v & 2) != 0; }
+// Sign of the stored accumulator of target v with the two-chain recurrence:
+// targets 2j and 2j+1 carry the sign s_j = (+, -, -, +, ...) of their chains.
+__host__ __device__ constexpr bool two_chain_negated(int v) { return ((v >> 1) & 3) == 1 || ((v >> 1) & 3) == 2; }
 
 // Equal-spacing recurrence.  When a thread's kV consecutive targets satisfy
 // b_v = b_0 + v*d exactly, exp(i 2 pi a.b_v) = exp(i 2 pi a.b_0) * u^v with
@@ -491,7 +494,7 @@ __host__ __device__ constexpr bool strided_negated(int v) { return (v & 2) != 0;
 // -2 cos first), so each target costs one packed FMA for the step and one
 // packed add into its accumulator, which holds s_v times the sum.  Voxels of a
 // regular image grid, and samples along a radial spoke, are equally spaced.
-template <int MODE>
+template <int MODE, bool TWO>
 __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict__ rec, float x0, float y0,
                                                         float z0, float dx, float dy, float dz, f2_t (&acc)[kV]) {
 #pragma unroll
@@ -518,18 +521,44 @@ __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict
         const float fi = fmaf(r1.z, s0, r1.w * c0);
         const float gr = fmaf(fr, cw, -fi * sw);      // g_1 = g_0 u
         const float gi = fmaf(fr, sw, fi * cw);
-        const float c2 = cw + cw;
-        const f2_t kpos = f2_pack(c2, c2), kneg = f2_pack(-c2, -c2);
-        f2_t em = f2_pack(fr, fi);  // e_{v-1}
-        f2_t e = f2_pack(gr, gi);   // e_v
-        acc[0] = f2_add(acc[0], em);
-        acc[1] = f2_add(acc[1], e);
+        if constexpr (TWO) {
+            const float c2 = cw + cw;
+            const f2_t kpos = f2_pack(c2, c2);
+            const f2_t e0 = f2_pack(fr, fi), e1 = f2_pack(gr, gi);
+            const f2_t e2n = f2_fma(f2_pack(-c2, -c2), e1, e0);  // -e_2
+            const f2_t e3n = f2_fma(kpos, e2n, e1);              // -e_3
+            const float cc = fmaf(c2, c2, -2.0f);                 // 2 cos(2 theta_d)
+            const f2_t kposC = f2_pack(cc, cc), knegC = f2_pack(-cc, -cc);
+            f2_t amA = e0, aA = e2n, amB = e1, aB = e3n;           // chains over even and odd targets
+            acc[0] = f2_add(acc[0], e0);
+            acc[1] = f2_add(acc[1], e1);
+            acc[2] = f2_add(acc[2], e2n);
+            acc[3] = f2_add(acc[3], e3n);
 #pragma unroll
-        for (int v = 1; v + 1 < kV; ++v) {
-            const f2_t en = f2_fma((v & 1) ? kneg : kpos, e, em);  // e_{v+1}
-            em = e;
-            e = en;
-            acc[v + 1] = f2_add(acc[v + 1], e);
+            for (int j = 1; 2 * j + 3 < kV; ++j) {
+                const f2_t nA = f2_fma((j & 1) ? kposC : knegC, aA, amA);  // s_{j+1} a_{j+1}
+                const f2_t nB = f2_fma((j & 1) ? kposC : knegC, aB, amB);
+                amA = aA;
+                aA = nA;
+                amB = aB;
+                aB = nB;
+                acc[2 * j + 2] = f2_add(acc[2 * j + 2], aA);
+                acc[2 * j + 3] = f2_add(acc[2 * j + 3], aB);
+            }
+        } else {
+            const float c2 = cw + cw;
+            const f2_t kpos = f2_pack(c2, c2), kneg = f2_pack(-c2, -c2);
+            f2_t em = f2_pack(fr, fi);  // e_{v-1}
+            f2_t e = f2_pack(gr, gi);   // e_v
+            acc[0] = f2_add(acc[0], em);
+            acc[1] = f2_add(acc[1], e);
+#pragma unroll
+            for (int v = 1; v + 1 < kV; ++v) {
+                const f2_t en = f2_fma((v & 1) ? kneg : kpos, e, em);  // e_{v+1}
+                em = e;
+                e = en;
+                acc[v + 1] = f2_add(acc[v + 1], e);
+            }
         }
     }
 }
@@ -567,17 +596,27 @@ __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* _
             const float gr = fmaf(fr, cw, -fi * sw);      // g_1 = g_0 u
             const float gi = fmaf(fr, sw, fi * cw);
             const float c2 = cw + cw;
-            const f2_t kpos = f2_pack(c2, c2), kneg = f2_pack(-c2, -c2);
-            f2_t em = f2_pack(fr, fi);  // e_{v-1}
-            f2_t e = f2_pack(gr, gi);   // e_v
-            acc[0] = f2_add(acc[0], em);
-            acc[1] = f2_add(acc[1], e);
+            const f2_t kpos = f2_pack(c2, c2);
+            const f2_t e0 = f2_pack(fr, fi), e1 = f2_pack(gr, gi);
+            const f2_t e2n = f2_fma(f2_pack(-c2, -c2), e1, e0);  // -e_2
+            const f2_t e3n = f2_fma(kpos, e2n, e1);              // -e_3
+            const float cc = fmaf(c2, c2, -2.0f);                 // 2 cos(2 theta_d)
+            const f2_t kposC = f2_pack(cc, cc), knegC = f2_pack(-cc, -cc);
+            f2_t amA = e0, aA = e2n, amB = e1, aB = e3n;           // chains over even and odd targets
+            acc[0] = f2_add(acc[0], e0);
+            acc[1] = f2_add(acc[1], e1);
+            acc[2] = f2_add(acc[2], e2n);
+            acc[3] = f2_add(acc[3], e3n);
 #pragma unroll
-            for (int v = 1; v + 1 < kV; ++v) {
-                const f2_t en = f2_fma((v & 1) ? kneg : kpos, e, em);  // e_{v+1}
-                em = e;
-                e = en;
-                acc[v + 1] = f2_add(acc[v + 1], e);
+            for (int j = 1; 2 * j + 3 < kV; ++j) {
+                const f2_t nA = f2_fma((j & 1) ? kposC : knegC, aA, amA);  // s_{j+1} a_{j+1}
+                const f2_t nB = f2_fma((j & 1) ? kposC : knegC, aB, amB);
+                amA = aA;
+                aA = nA;
+                amB = aB;
+                aB = nB;
+                acc[2 * j + 2] = f2_add(acc[2 * j + 2], aA);
+                acc[2 * j + 3] = f2_add(acc[2 * j + 3], aB);
             }
         }
     }
@@ -585,7 +624,7 @@ __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* _
 
 // One staged tile on the target-side recurrence, folded into the thread's
 // running sums (the signs of the stored terms undone here).
-template <int MODE>
+template <int MODE, bool TWO>
 __device__ __forceinline__ void strided_tile(const float4* __restrict__ rec, float x0, float y0, float z0,
                                              float dx, float dy, float dz, int lane, bool shared_u,
                                              float (*run)[kThreads], int tid) {
@@ -593,12 +632,12 @@ __device__ __forceinline__ void strided_tile(const float4* __restrict__ rec, flo
     if (MODE == kAccurate && shared_u)
         accumulate_tile_strided_shared_u(rec, x0, y0, z0, dx, dy, dz, lane, acc);
     else
-        accumulate_tile_strided<MODE>(rec, x0, y0, z0, dx, dy, dz, acc);
+        accumulate_tile_strided<MODE, TWO>(rec, x0, y0, z0, dx, dy, dz, acc);
 #pragma unroll
     for (int v = 0; v < kV; ++v) {
         float re, im;
         f2_unpack(acc[v], re, im);
-        if (strided_negated(v)) {
+        if (TWO ? two_chain_negated(v) : strided_negated(v)) {
             run[v][tid] -= re;
             run[kV + v][tid] -= im;
         } else {
@@ -757,6 +796,11 @@ __device__ __noinline__ void accumulate_tile_src_strided_ool(const float4* __res
 template <int MODE, int NPOLY, int SEG>
 __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(const GatherArgs args) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
+    // The target-side recurrence runs as two chains (even and odd targets),
+    // except in the fast forward gather, where a single chain measured faster
+    // (its targets, the samples, rarely take the recurrence at all).
+    constexpr bool kTwoChains = !(MODE == kFast && SEG == kSegmentAccurate);
+    static_assert(MODE == kFast || kTwoChains, "the accurate kernel's fold assumes two chains");
     GatherSmem& sm = *reinterpret_cast<GatherSmem*>(smem_raw);
 
     // A set skip word (written by an earlier kernel on the stream, never while
@@ -871,18 +915,18 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
         const float4* rec = &sm.ring[st][0];
         if (strided) {
             if constexpr (MODE == kFast) {
-                strided_tile<MODE>(rec, x0, y0, z0, sx, sy, sz, lane, shared_u, sm.run, tid);
+                strided_tile<MODE, kTwoChains>(rec, x0, y0, z0, sx, sy, sz, lane, shared_u, sm.run, tid);
             } else {
                 f2_t acc[kV];
                 if (shared_u)
                     accumulate_tile_strided_shared_u(rec, x0, y0, z0, sx, sy, sz, lane, acc);
                 else
-                    accumulate_tile_strided<MODE>(rec, x0, y0, z0, sx, sy, sz, acc);
+                    accumulate_tile_strided<MODE, kTwoChains>(rec, x0, y0, z0, sx, sy, sz, acc);
 #pragma unroll
                 for (int v = 0; v < kV; ++v) {
                     float re, im;
                     f2_unpack(acc[v], re, im);
-                    if (strided_negated(v)) {
+                    if (two_chain_negated(v)) {  // the accurate kernel always uses two chains
                         sm.run[v][tid] -= re;
                         sm.run[kV + v][tid] -= im;
                     } else {

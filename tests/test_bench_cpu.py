@@ -30,8 +30,8 @@ def test_roofline_counts():
     assert 16 / mufu < min(128 / lanes, 128 / issue)
     lanes, mufu, issue = bench.per_pair_counts("recurrence")
     V = bench.TARGETS_PER_THREAD
-    assert abs(lanes - (4 - 4 / V + 15 / V)) < 1e-12 and abs(mufu - 4 / V) < 1e-12
-    assert abs(issue - (2 + 14 / V)) < 1e-12
+    assert abs(lanes - (4 - 4 / V + 16 / V)) < 1e-12 and abs(mufu - 4 / V) < 1e-12
+    assert abs(issue - (2 + 15 / V)) < 1e-12
     # with V = 32 the FP32 lanes bind
     assert abs(bench.peak_pairs_per_s(152, 2070.0, "recurrence") - 152 * (128 / lanes) * 2070e6) < 1
 
