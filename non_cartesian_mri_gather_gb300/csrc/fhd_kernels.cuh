@@ -101,7 +101,11 @@ constexpr int kCtaThreads = kThreads + 32;  // + one producer warp
 constexpr int kMinCtasPerSm = FHD_MIN_CTAS_PER_SM;
 constexpr int kUnroll = FHD_UNROLL;      // sources per unrolled inner-loop step
 constexpr int kUnrollSharedU = 8;        // the same in the accurate warp-shared-phasor loop (measured best)
-constexpr int kUnrollStrided = 3;        // and in the target-side recurrence's sample loop (measured best)
+// and in the target-side recurrence's sample loop (measured best): two
+// chains (the fast adjoint and the accurate kernels), one chain (the fast
+// forward kernel)
+constexpr int kUnrollTwoChains = 5;
+constexpr int kUnrollOneChain = 3;
 static_assert(kThreads % 32 == 0 && kTile % 2 == 0 && kStages >= 2, "bad launch shape");
 
 // status word bits
@@ -501,7 +505,8 @@ __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict
 #pragma unroll
     for (int v = 0; v < kV; ++v) acc[v] = 0ull;  // +0.0f in both halves
     const f2_t bx = f2_pack(x0, dx), by = f2_pack(y0, dy), bz = f2_pack(z0, dz);
-#pragma unroll kUnrollStrided
+    constexpr int kU = TWO ? kUnrollTwoChains : kUnrollOneChain;
+#pragma unroll kU
     for (int s = 0; s < kTile; ++s) {
         const float4 r0 = rec[2 * s];      // A.x A.x A.y A.y
         const float4 r1 = rec[2 * s + 1];  // A.z A.z w.re w.im
