@@ -31,14 +31,38 @@ def host_complex(re, im) -> np.ndarray:
     return re.detach().cpu().numpy().astype(np.float64) + 1j * im.detach().cpu().numpy().astype(np.float64)
 
 
-def sample_indices(n: int, count: int, seed: int = 0) -> np.ndarray:
-    """A fixed spread of indices: evenly strided plus the first and last few."""
+def sample_indices(n: int, count: int, run: int = 32, block: int = 8192) -> np.ndarray:
+    """About `count` indices spread over [0, n), chosen so that every part of
+    the gather's target layout is checked.
+
+    - An odd stride: coprime with every power of two, so the sample meets
+      every position 0..run-1 of a thread's run of `run` consecutive targets
+      about equally often (the recurrence's anchor at position 0 and every
+      chained target after it), and every residue of a power-of-two row
+      length (both row ends).
+    - The first and last `run` targets of the first, a middle and the last
+      target block of `block` targets (block edges, the ragged last block).
+    - The last `run` targets.
+    """
     if n <= count:
         return np.arange(n)
     stride = max(1, n // count)
-    idx = np.arange(0, n, stride)[:count]
-    tail = np.arange(max(0, n - 5), n)
-    return np.unique(np.concatenate([idx, np.arange(5), tail]))
+    if stride % 2 == 0:
+        stride -= 1
+    idx = [np.arange(0, n, stride)[:count]]
+    last_block = ((n - 1) // block) * block
+    for b0 in sorted({0, ((n // block) // 2) * block, last_block}):
+        idx.append(np.arange(b0, min(n, b0 + run)))
+        idx.append(np.arange(max(0, b0 + block - run), min(n, b0 + block)))
+    idx.append(np.arange(max(0, n - run), n))
+    return np.unique(np.concatenate(idx))
+
+
+def rel_l2_by_position(got, ref, idx, run: int = 32) -> dict:
+    """Relative L2 error over the sampled targets at each position idx % run
+    of a thread's run of consecutive targets."""
+    got, ref, pos = np.asarray(got), np.asarray(ref), np.asarray(idx) % run
+    return {int(q): rel_l2(got[pos == q], ref[pos == q]) for q in range(run) if np.any(pos == q)}
 
 
 def gpu_fhd(p, mode, ws=None):

@@ -23,7 +23,7 @@ import pytest
 import oracle
 from inputs import make_workload, random_problem
 from tests.gpu_helpers import (PATH_AUTO, PATH_PERSISTENT, PSNR_FAST_DB, TOL_ACCURATE, TOL_FAST, gather_path, gpu_fhd,
-                               gpu_fhf, gpu_fwd, psnr_db, rel_l2, sample_indices)
+                               gpu_fhf, gpu_fwd, psnr_db, rel_l2, rel_l2_by_position, sample_indices)
 
 pytestmark = pytest.mark.gpu
 
@@ -127,24 +127,44 @@ def ref2():
 @pytest.mark.auto_path
 @pytest.mark.parametrize("mode", ALL_MODES)
 def test_workload2_full(mode, ref2):
-    check(gpu_fhd(workload(2), mode), ref2, mode, "workload 2")
+    got = gpu_fhd(workload(2), mode)
+    check(got, ref2, mode, "workload 2")
+    check_by_position(got, ref2, np.arange(got.size), mode, f"workload 2 mode {mode}")
+
+
+def check_by_position(got, ref, idx, mode, what):
+    """The relative L2 error at each position of a thread's 32-target run
+    (sampled targets idx), each within the mode's tolerance; prints them."""
+    errs = rel_l2_by_position(got, ref, idx)
+    worst = max(errs, key=errs.get)
+    print(f"{what}: worst position {worst} relL2 {errs[worst]:.3e}; by position "
+          + " ".join(f"{q}:{e:.2e}" for q, e in sorted(errs.items())))
+    tol = TOL_ACCURATE if (mode & 1) == 0 else TOL_FAST
+    assert errs[worst] <= tol, f"{what}: position {worst} relL2 {errs[worst]:.3e}"
+    return errs
 
 
 @pytest.mark.auto_path
 @pytest.mark.parametrize("wl", [3, 4])
 @pytest.mark.parametrize("mode", [ACC, FAST])
 def test_workload_sampled(wl, mode):
+    """Workloads 3 and 4 on about 4300 voxels: an odd stride meets every
+    position of a thread's 32-voxel recurrence run about 134 times, plus the
+    edges of three target blocks; each position's relL2 is checked."""
     p = workload(wl)
     got = gpu_fhd(p, mode)
     idx = sample_indices(p.N, 4096)
     ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x[idx], p.y[idx], p.z[idx])
     check(got[idx], ref, mode, f"workload {wl} ({idx.size} sampled voxels)")
+    check_by_position(got[idx], ref, idx, mode, f"workload {wl} mode {mode}")
 
 
 @pytest.mark.auto_path
 @pytest.mark.parametrize("mode", [ACC, FAST])
 def test_workload5(mode):
-    """F^H F rho at 128^3 x 262144: forward pass on sampled samples vs the oracle,
+    """F^H F rho at 128^3 x 262144: the forward pass on sampled samples and the
+    adjoint pass on sampled voxels against the oracle (the adjoint pass is fed
+    the GPU's own float32 F rho, which is exactly what the second pass reads),
     the composed operator equal to fhd_compute(fwd_compute(rho)) bit for bit,
     and <rho, F^H F rho> = ||F rho||^2 (real, positive)."""
     import torch
@@ -165,10 +185,48 @@ def test_workload5(mode):
     ref = oracle.forward(p.x, p.y, p.z, rho, p.kx[idx], p.ky[idx], p.kz[idx])
     check(Frho[idx], ref, mode, "workload 5 forward pass (sampled samples)")
     out = host_complex(o_r, o_i)
+    vox = sample_indices(p.N, 4096)
+    ref2 = oracle.adjoint(p.kx, p.ky, p.kz, Frho, p.x[vox], p.y[vox], p.z[vox])
+    check(out[vox], ref2, mode, f"workload 5 adjoint pass ({vox.size} sampled voxels)")
+    check_by_position(out[vox], ref2, vox, mode, f"workload 5 adjoint pass mode {mode}")
     q = np.vdot(rho.astype(np.complex128), out)
     nrm = np.vdot(Frho, Frho).real
     assert abs(q.imag) <= 1e-4 * abs(q.real)
     assert abs(q.real - nrm) <= (1e-4 if mode == ACC else 1e-2) * nrm
+
+
+# ------------------------------------------------------------ large |k.x|
+
+@pytest.mark.parametrize("kmax", [1024.0, 4096.0])
+@pytest.mark.parametrize("coords", ["uniform", "grid"])
+@pytest.mark.parametrize("mode", ALL_MODES)
+def test_fhd_large_k(kmax, coords, mode):
+    """k uniform in [-kmax, kmax)^3 cycles per FOV on a unit FOV, so |k.x|
+    reaches about 0.87 kmax cycles (3500 at kmax = 4096), on scattered voxels
+    and on a 32^3 grid (the recurrences).  Every sin/cos follows the range
+    reduction: fast mode stays within 1e-3 (its float32 phase, one FMA chain,
+    carries a rounding error growing with |k.x|: about 6.5e-8 kmax in relative
+    L2), accurate mode within 1e-5 (each product reduced on its own)."""
+    p = random_problem(32768 if coords == "grid" else 9000, 1500, kmax=kmax, seed=int(kmax) + len(coords),
+                       coords=coords)
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    err = check(gpu_fhd(p, mode), ref, mode, f"F^H D kmax={kmax:g} {coords}")
+    print(f"F^H D kmax={kmax:g} {coords} mode {mode}: relL2 {err:.3e}")
+
+
+@pytest.mark.parametrize("kmax", [1024.0, 4096.0])
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_fwd_large_k(kmax, mode):
+    """F rho with the voxels of a 32^3 grid as sources (the source-side
+    recurrence) and samples up to kmax cycles per FOV."""
+    from inputs import grid_coords
+
+    x, y, z = grid_coords(32, 32, 32)
+    p = random_problem(x.size, 1200, kmax=kmax, seed=int(kmax) + 1, op="fwd")
+    p.x, p.y, p.z = x, y, z
+    ref = oracle.forward(p.x, p.y, p.z, p.rho_r + 1j * p.rho_i, p.kx, p.ky, p.kz)
+    err = check(gpu_fwd(p, mode), ref, mode, f"F rho kmax={kmax:g}")
+    print(f"F rho kmax={kmax:g} mode {mode}: relL2 {err:.3e}")
 
 
 # ------------------------------------------------------------ equal-spacing recurrence
