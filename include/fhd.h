@@ -47,12 +47,25 @@
  *            time limit (about one second) records FHD_ERR_TIMEOUT in the
  *            workspace status word and exits early; read it with
  *            fhd_workspace_status() after synchronising.
- * Modes      FHD_MODE_ACCURATE evaluates sin/cos with sincospif on the
- *            period-reduced phase (relative L2 error vs an fp64 evaluation
- *            below 1e-5 on the benchmark workloads).  FHD_MODE_FAST uses the
- *            hardware sin/cos approximations, partly replaced by an FMA-pipe
- *            polynomial (relative L2 error below 1e-3).  Either may be OR-ed
- *            with FHD_MODE_DIRECT, see below.
+ * Modes      Phases are in cycles, and every sin/cos follows the range
+ *            reduction t = k.x - rint(k.x).
+ *            FHD_MODE_ACCURATE forms each pair's reduced phase from the
+ *            three products k_j x_j reduced one by one (error below 2e-7
+ *            cycles for any |k.x| < 2^21) and evaluates sin/cos with an
+ *            FMA-pipe minimax polynomial (error below 2.4e-7); the step
+ *            phasors of the equal-spacing recurrences use sincospif.
+ *            Relative L2 error against an fp64 evaluation: below 2e-6 on
+ *            the benchmark workloads, and within 1e-5 up to |k| = 4096
+ *            cycles/FOV on a unit FOV (tested).
+ *            FHD_MODE_FAST forms the phase as one float32 FMA chain, whose
+ *            rounding grows with |k.x| (relative L2 error about
+ *            6.5e-8 * max|k| for k uniform in a cube on a unit FOV: 3e-4 at
+ *            |k| = 4096, below 2e-5 on the benchmark workloads), and uses
+ *            the hardware sin/cos approximations on 2 pi t in [-pi, pi],
+ *            partly replaced by an FMA-pipe polynomial.  Relative L2 error
+ *            3.3e-4 measured at |k| = 4096 (|k.x| up to 3500 cycles); it grows
+ *            in proportion to |k.x| and reaches 1e-3 near 1e4 cycles.
+ *            Either may be OR-ed with FHD_MODE_DIRECT, see below.
  * Spacing    where a thread's 32 consecutive targets (voxels for F^H D,
  *            samples for F rho) are exactly equally spaced, as the voxels of a
  *            regular image grid are, the kernel evaluates two phasors per

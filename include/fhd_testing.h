@@ -1,9 +1,11 @@
 /*
- * fhd_testing.h - test-only entry point of the fhd library.
+ * fhd_testing.h - test-only entry points of the fhd library.
  *
- * Not part of the operator API in fhd.h; it exists so the test-suite can
- * exercise the bounded-wait failure path without faulting or hanging a GPU.
- * The library has no counterpart of this on the pages it implements.
+ * Not part of the operator API in fhd.h; they exist so the test-suite can
+ * exercise the bounded-wait failure path without faulting or hanging a GPU,
+ * force or inspect the gather path, replay the schedule on the host, check
+ * pointers without launching, and check the per-pair phasor on its own.
+ * The library has no counterpart of these on the pages it implements.
  */
 #ifndef FHD_TESTING_H
 #define FHD_TESTING_H
@@ -75,6 +77,27 @@ FHD_API int fhd_test_schedule(int64_t n_targets, int64_t n_sources, int ctas);
  * nothing, so a rejected pointer is never dereferenced.
  */
 FHD_API fhd_status fhd_test_check_array(const void *p, size_t bytes, int device);
+
+/*
+ * The per-pair phasor of the sums, evaluated on its own: for i < n, the
+ * phase p_i = ax_i bx_i + ay_i by_i + az_i bz_i (in cycles) and
+ * s_i, c_i ~= sin(2 pi p_i), cos(2 pi p_i) by the method `which` selects:
+ *   0  accurate mode: the compensated reduced phase (each product reduced on
+ *      its own) and the accurate FMA-pipe polynomial, as every accurate path
+ *      evaluates a pair;
+ *   1  fast mode, hardware sin/cos: p as one float32 FMA chain, reduced to
+ *      t = p - rint(p), sin/cos of 2 pi t on the MUFU pipe;
+ *   2  fast mode, FMA-pipe share: the same p, the fast polynomial;
+ *   3  CUDA's sincospif(2 t) of the t of method 1 (a reference for 4);
+ *   4  the accurate polynomial of the t of method 1.
+ * All arrays are float32 device arrays of n elements (inputs ax..bz, outputs
+ * s, c), 4-byte aligned; the call validates them as the operators do and
+ * returns FHD_ERR_INVALID_VALUE for an unknown `which` or n < 0.  Enqueued on
+ * `stream`, asynchronous.
+ */
+FHD_API fhd_status fhd_test_phasor(int which, int64_t n, const float *ax, const float *ay, const float *az,
+                                   const float *bx, const float *by, const float *bz, float *s, float *c,
+                                   fhd_stream_t stream);
 
 #ifdef __cplusplus
 }

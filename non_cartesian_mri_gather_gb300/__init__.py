@@ -102,6 +102,7 @@ SIGNATURES = {
     "fhd_test_split_shape": (_int, [_i64, _i64, _int, _int, _sz, ctypes.POINTER(ctypes.c_int),
                                     ctypes.POINTER(ctypes.c_int64)]),
     "fhd_test_check_array": (_int, [_vp, _sz, _int]),
+    "fhd_test_phasor": (_int, [_int, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 
 

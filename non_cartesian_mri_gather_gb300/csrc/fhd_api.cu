@@ -174,7 +174,7 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     const int64_t padded = sch.n_tiles * kTile;
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    const float scale = g.sign * (fast_mode(mode) ? 6.28318530717958647692f : 1.0f);
+    const float sign = g.sign;  // phases in cycles in both modes
 
     const SplitShape split = split_shape(g.n_targets, g.n_sources, sms, ctas_max, L.frho - L.partial);
     bool use_split = split.worth_it;
@@ -188,11 +188,11 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
         const dim3 grid((unsigned)ceil_div(g.n_targets, kSplitThreads), (unsigned)split.n_slices);
         if (fast_mode(mode))
             split_gather_kernel<kFast><<<grid, kSplitThreads, 0, stream>>>(
-                g.tx, g.ty, g.tz, g.n_targets, g.sx, g.sy, g.sz, g.wr, g.wi, scale, g.n_sources, split.slice_len,
+                g.tx, g.ty, g.tz, g.n_targets, g.sx, g.sy, g.sz, g.wr, g.wi, sign, g.n_sources, split.slice_len,
                 partial, g.out_r, g.out_i, status, first_pass ? 1 : 0, skip);
         else
             split_gather_kernel<kAccurate><<<grid, kSplitThreads, 0, stream>>>(
-                g.tx, g.ty, g.tz, g.n_targets, g.sx, g.sy, g.sz, g.wr, g.wi, scale, g.n_sources, split.slice_len,
+                g.tx, g.ty, g.tz, g.n_targets, g.sx, g.sy, g.sz, g.wr, g.wi, sign, g.n_sources, split.slice_len,
                 partial, g.out_r, g.out_i, status, first_pass ? 1 : 0, skip);
         if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
         if (split.n_slices > 1) {
@@ -205,7 +205,7 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     }
 
     const int pack_grid = (int)std::min<int64_t>(ceil_div(padded, 256), (int64_t)sms * 8);
-    pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, scale, g.n_sources, padded,
+    pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, sign, g.n_sources, padded,
                                                 packed, status, first_pass ? 1 : 0, skip);
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
 
@@ -216,10 +216,10 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     const int64_t n_segments = padded / (long_segments ? kSegmentAccurate : kSegment);
     const int desc_grid = (int)std::min<int64_t>(ceil_div(n_segments, 256), (int64_t)sms * 8);
     if (long_segments)
-        describe_segments<kSegmentAccurate><<<desc_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, scale, g.n_sources,
+        describe_segments<kSegmentAccurate><<<desc_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, sign, g.n_sources,
                                                                            n_segments, desc, skip);
     else
-        describe_segments<kSegment><<<desc_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, scale, g.n_sources, n_segments,
+        describe_segments<kSegment><<<desc_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, sign, g.n_sources, n_segments,
                                                                    desc, skip);
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
 
@@ -533,6 +533,64 @@ fhd_status fhd_compute_noalloc(int64_t M, const float* kx, const float* ky, cons
     if (s != FHD_OK) return s;
     return fhd_compute_impl(M, kx, ky, kz, Dr, Di, N, x, y, z, rho_r, rho_i, mode, scratch, kNoAllocScratchBytes,
                             (cudaStream_t)stream, nullptr, nullptr, -1);
+}
+
+}  // extern "C"
+
+namespace fhd {
+namespace {
+
+// fhd_test_phasor: one thread per pair, the methods listed in fhd_testing.h.
+__global__ void test_phasor_kernel(int which, int64_t n, const float* __restrict__ ax, const float* __restrict__ ay,
+                                   const float* __restrict__ az, const float* __restrict__ bx,
+                                   const float* __restrict__ by, const float* __restrict__ bz, float* __restrict__ s,
+                                   float* __restrict__ c) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float sn = 0.f, cs = 0.f;
+        const float p = fmaf(az[i], bz[i], fmaf(ay[i], by[i], ax[i] * bx[i]));
+        const float t = p - rint_fma(p);
+        switch (which) {
+            case 0: phasor_accurate(ax[i], ay[i], az[i], bx[i], by[i], bz[i], sn, cs); break;
+            case 1: phasor_mufu(p, sn, cs); break;
+            case 2: sincos2pi_poly<false>(p, sn, cs); break;
+            case 3: sincospif(2.0f * t, &sn, &cs); break;
+            default: sincos2pi_poly<true>(t, sn, cs); break;
+        }
+        s[i] = sn;
+        c[i] = cs;
+    }
+}
+
+}  // namespace
+}  // namespace fhd
+
+extern "C" {
+
+// Declared in include/fhd_testing.h.
+fhd_status fhd_test_phasor(int which, int64_t n, const float* ax, const float* ay, const float* az, const float* bx,
+                           const float* by, const float* bz, float* s, float* c, fhd_stream_t stream) {
+    if (which < 0 || which > 4 || n < 0) return FHD_ERR_INVALID_VALUE;
+    if (n == 0) return FHD_OK;
+    const size_t b = (size_t)n * sizeof(float);
+    const Buf ins[] = {{ax, b}, {ay, b}, {az, b}, {bx, b}, {by, b}, {bz, b}};
+    const Buf outs[] = {{s, b}, {c, b}};
+    for (const Buf& o : outs)
+        for (const Buf& in : ins)
+            if (overlaps(o, in)) return FHD_ERR_ALIAS;
+    if (overlaps(outs[0], outs[1])) return FHD_ERR_ALIAS;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) {
+        cudaGetLastError();
+        return FHD_ERR_CUDA;
+    }
+    fhd_status st;
+    for (const Buf& a : ins)
+        if ((st = check_array(a.p, a.bytes, 4, device)) != FHD_OK) return st;
+    for (const Buf& a : outs)
+        if ((st = check_array(a.p, a.bytes, 4, device)) != FHD_OK) return st;
+    const int grid = (int)std::min<int64_t>(ceil_div(n, 256), 4096);
+    test_phasor_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(which, n, ax, ay, az, bx, by, bz, s, c);
+    return cuda_status(cudaGetLastError());
 }
 
 // Declared in include/fhd_testing.h.

@@ -16,7 +16,8 @@
 //   1. pack_sources   - loop fission / per-source precompute (section 17.3.2):
 //                       SoA source arrays -> 32-byte AoS records
 //                       {A.x, A.x, A.y, A.y, A.z, A.z, w.re, w.im} (A the
-//                       scaled source coordinates), padded with zero-weight
+//                       source coordinates, negated for the forward sum),
+//                       padded with zero-weight
 //                       records to a whole number of tiles.  The
 //                       array-of-structures record follows the mtuann notes'
 //                       step 4 and the SampleChunk struct of section 17.3.4.
@@ -116,7 +117,7 @@ constexpr uint32_t kStatusDrainTimeout = 4u;
 enum Mode : int { kAccurate = 0, kFast = 1 };
 // Source segments are kSegment sources long in fast mode and
 // kSegmentAccurate in accurate mode, where the longer segment halves the
-// per-(target, segment) sincospif cost of the source-side recurrence (its
+// per-(target, segment) sin/cos cost of the source-side recurrence (its
 // three-term error bound, eps * s^2 / 2, stays below 3e-5 over 32 sources);
 // the descriptor array is sized for kSegment.
 constexpr int kSegmentAccurate = 32;
@@ -131,7 +132,7 @@ __host__ __device__ constexpr int segment_len() {
 // The pair-by-pair path walks a thread's kV targets in groups (coordinates and
 // per-tile sums of one group in registers at a time): wider in fast mode,
 // where more independent MUFU operations per warp hide their latency, than in
-// accurate mode, whose sincospif needs the registers.
+// accurate mode, whose compensated phase and polynomial need the registers.
 #ifndef FHD_DIRECT_GROUP
 #define FHD_DIRECT_GROUP 16
 #endif
@@ -275,62 +276,123 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 }
 
 // ---------------------------------------------------------------- per-pair math
-// Rounding to the nearest integer with the FMA pipe: for |v| < 2^22,
-// (v + 1.5*2^23) - 1.5*2^23 == rint(v) in round-to-nearest-even (the sum's ulp
-// is 1).  rintf() itself issues on the same 16-lane/SM/clock pipe as the
-// hardware sin/cos approximations on this GPU, so it is avoided.
+// Phases are in cycles in both modes: the packed source coordinates are the
+// caller's, unscaled (k in cycles per FOV, or -x for the forward sum), and the
+// phasor of a pair is exp(i 2 pi p) with p = a.b.  Every sin/cos follows the
+// range reduction t = p - rint(p) ("Case study - iterative MRI
+// reconstruction", section 17.3.5: the hardware sin/cos lose accuracy once
+// 2 pi has been multiplied into a large argument), so the hardware
+// approximations only ever see 2 pi t in [-pi, pi], the interval on which
+// they are specified.
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr float kTwoPi = 6.28318530717958647692f;
 
-// Accurate mode (phase p in cycles): t = p - rint(p) is exact in fp32 for
-// |p| < 2^22, and sincospif(2t) gives sin, cos of 2 pi t.
-__device__ __forceinline__ void phasor_accurate(float p, float& s, float& c) {
-    const float r = (p + kRoundMagic) - kRoundMagic;
-    const float t = p - r;
-    sincospif(2.0f * t, &s, &c);
+// rint(v) on the FMA pipe: for |v| < 2^22, (v + 1.5*2^23) - 1.5*2^23 == rint(v)
+// in round-to-nearest-even (the sum's ulp is 1).  rintf() itself issues on
+// the 16-lane/SM/clock pipe of the hardware sin/cos approximations, so it is
+// used only where that pipe has room: the recurrences (4 sin/cos per 32
+// pairs) and the accurate mode (no hardware sin/cos at all).
+__device__ __forceinline__ float rint_fma(float v) { return (v + kRoundMagic) - kRoundMagic; }
+
+// Fast mode, MUFU pipe: t = p - rint(p) in [-1/2, 1/2] (exact in float32 for
+// |p| < 2^22), then the hardware sin/cos of 2 pi t.
+__device__ __forceinline__ void phasor_mufu(float p, float& s, float& c) {
+    const float th = kTwoPi * (p - rint_fma(p));
+    s = __sinf(th);
+    c = __cosf(th);
 }
 
-// Fast mode, MUFU pipe (phase P in radians: 2 pi is folded into the packed
-// source coordinates): hardware sin/cos approximations.  The argument is not
-// reduced; the fp32 rounding of P (|P| up to a few hundred radians for the
-// supported k ranges) stays far below the fast-mode tolerance.
-__device__ __forceinline__ void phasor_mufu(float P, float& s, float& c) {
-    s = __sinf(P);
-    c = __cosf(P);
+// sin(2 pi t), cos(2 pi t) on the FMA pipe, for |t| < 2^21: the half-period
+// reduction n = rint(2t), u = t - n/2 in [-1/4, 1/4] (exact), the minimax
+// polynomials of sincos_poly.cuh in u, and the sign (-1)^n on both results (a
+// shift by half a period flips both).  The parity of n is the low mantissa bit
+// of 2t + 1.5*2^23, whose ulp is 1.  ACC selects the accurate coefficient set
+// (max error 2.4e-7) or the fast one (7.6e-7).
+template <bool ACC>
+__device__ __forceinline__ void sincos2pi_poly(float t, float& s, float& c) {
+    const float q = fmaf(t, 2.0f, kRoundMagic);
+    const float u = fmaf(q - kRoundMagic, -0.5f, t);
+    const uint32_t flip = __float_as_uint(q) << 31;
+    const float w = u * u;
+    float sn, pc;
+    if constexpr (ACC) {
+        float ps = poly::kAccurateSin[poly::kAccurateSinTerms - 1];
+#pragma unroll
+        for (int i = poly::kAccurateSinTerms - 2; i >= 1; --i) ps = fmaf(ps, w, poly::kAccurateSin[i]);
+        sn = fmaf(poly::kAccurateSin[0], u, (u * w) * ps);  // the leading term's product exact in the FMA
+        pc = poly::kAccurateCos[poly::kAccurateCosTerms - 1];
+#pragma unroll
+        for (int i = poly::kAccurateCosTerms - 2; i >= 0; --i) pc = fmaf(pc, w, poly::kAccurateCos[i]);
+    } else {
+        float ps = poly::kFastSin[poly::kFastSinTerms - 1];
+#pragma unroll
+        for (int i = poly::kFastSinTerms - 2; i >= 0; --i) ps = fmaf(ps, w, poly::kFastSin[i]);
+        sn = ps * u;
+        pc = poly::kFastCos[poly::kFastCosTerms - 1];
+#pragma unroll
+        for (int i = poly::kFastCosTerms - 2; i >= 0; --i) pc = fmaf(pc, w, poly::kFastCos[i]);
+    }
+    s = __uint_as_float(__float_as_uint(sn) ^ flip);
+    c = __uint_as_float(__float_as_uint(pc) ^ flip);
 }
 
-// Fast mode, FMA pipe (phase P in radians): theta = P - 2 pi rint(P / 2 pi) in
-// [-pi, pi] (one-constant reduction; its error is r * |2pi - fl(2pi)| <=
-// 2e-5 rad for |P| <= 700), then the half-angle polynomial of
-// sincos_poly.cuh: sin = S*C, cos = 1 - S*S.
-__device__ __forceinline__ void phasor_poly(float P, float& s, float& c) {
-    const float q = fmaf(P, 0.159154943091895335769f, kRoundMagic);
-    const float r = q - kRoundMagic;
-    const float th = fmaf(r, -6.28318530717958647692f, P);
-    const float w = th * th;
-    float ps = poly::kSin[poly::kSinTerms - 1];
-#pragma unroll
-    for (int i = poly::kSinTerms - 2; i >= 0; --i) ps = fmaf(ps, w, poly::kSin[i]);
-    const float S = ps * th;
-    float pc = poly::kCos[poly::kCosTerms - 1];
-#pragma unroll
-    for (int i = poly::kCosTerms - 2; i >= 0; --i) pc = fmaf(pc, w, poly::kCos[i]);
-    s = S * pc;
-    c = fmaf(-S, S, 1.0f);
+// Accurate mode: the reduced phase of a pair, compensated.  A phase formed as
+// one float32 dot product carries a rounding error that grows with |a.b|
+// (about 2^-24 |a.b| cycles: 6e-6 cycles at |a.b| = 100, the dominant error
+// of the sum on large grids).  Here each product is reduced on its own,
+// frac(a b) = a b - rint(fl(a b)) in one FMA: the product is exact inside the
+// FMA and only a result of magnitude at most 1/2 + ulp(a b)/2 is rounded,
+// within 2^-25 of the exact fraction.  Their sum t (|t| < 2) is within
+// 3e-7 cycles of a.b - rint(a.b) + an integer for any |a.b| < 2^22.
+__device__ __forceinline__ float frac_mul(float a, float b) { return fmaf(a, b, -rintf(a * b)); }
+
+__device__ __forceinline__ float phase_accurate(float ax, float ay, float az, float bx, float by, float bz) {
+    return (frac_mul(ax, bx) + frac_mul(ay, by)) + frac_mul(az, bz);
+}
+
+// Accurate mode: sin, cos of 2 pi a.b for the pair (a, b).
+__device__ __forceinline__ void phasor_accurate(float ax, float ay, float az, float bx, float by, float bz,
+                                                float& s, float& c) {
+    sincos2pi_poly<true>(phase_accurate(ax, ay, az, bx, by, bz), s, c);
+}
+
+// Accurate mode, the step phasor of a recurrence: sin, cos of 2 pi a.b with
+// sincospif on the compensated phase.  A recurrence rotates by the step's
+// angle once per target, so a relative error of that angle grows with the
+// target's position (31 steps), where an error of the anchor phasor only
+// scales every term alike: the step needs sin and cos correct to about an
+// ulp, which the polynomial (absolute error 2.4e-7, its slope at 0 off by
+// 1e-7 relative) does not give.  A step phasor is evaluated once per 32
+// pairs or fewer.
+__device__ __forceinline__ void phasor_step_accurate(float ax, float ay, float az, float bx, float by, float bz,
+                                                     float& s, float& c) {
+    sincospif(2.0f * phase_accurate(ax, ay, az, bx, by, bz), &s, &c);
+}
+
+// 2 cos(2 theta) from s = sin(theta), c = cos(theta), in the form that keeps
+// the precision of the inputs where the recurrence needs it: 2 - 4 s^2 where
+// 2 theta is near a multiple of 2 pi (the coefficient near 2), 4 c^2 - 2
+// where it is near an odd multiple of pi (near -2).  Near those ends the
+// angle a three-term recurrence turns by is most sensitive to its
+// coefficient, and the other form would carry 8 times the error of its
+// input there.
+__device__ __forceinline__ float two_cos_double(float s, float c) {
+    return fabsf(s) < fabsf(c) ? fmaf(-4.0f * s, s, 2.0f) : fmaf(4.0f * c, c, -2.0f);
 }
 
 // ---------------------------------------------------------------- pack
-// Source records {A.x, A.x, A.y, A.y, A.z, A.z, w.re, w.im} with A = scale*a:
-// each coordinate twice, so one 16-byte load gives (A.x, A.x, A.y, A.y) as the
-// packed pairs the recurrence multiplies by (x0, dx) and (y0, dy);
-// scale is +-1 (accurate mode, phase in cycles) or +-2 pi (fast mode, phase
-// in radians), negative for the forward sum.
+// Source records {A.x, A.x, A.y, A.y, A.z, A.z, w.re, w.im} with A = sign*a
+// (exact; sign is -1 for the forward sum, whose sources are the voxels, and +1
+// for the adjoint sum; phases are in cycles in both modes): each coordinate
+// twice, so one 16-byte load gives (A.x, A.x, A.y, A.y) as the packed pairs
+// the recurrence multiplies by (x0, dx) and (y0, dy).
 // Records n..n_padded-1 are zero (weight 0, so they add exactly 0).
 // With `reset_status`, block 0 thread 0 also clears the status word (stream
 // order puts this before the gather kernel); the second pass of F^H F rho
 // keeps the word so a timeout of the first pass stays visible.
 __global__ void pack_sources(const float* __restrict__ ax, const float* __restrict__ ay,
                              const float* __restrict__ az, const float* __restrict__ wr,
-                             const float* __restrict__ wi, float scale, int64_t n, int64_t n_padded,
+                             const float* __restrict__ wi, float sign, int64_t n, int64_t n_padded,
                              float4* __restrict__ out, uint32_t* status, int reset_status,
                              const uint32_t* skip) {
     if (skip != nullptr && *skip != 0u) return;
@@ -340,7 +402,7 @@ __global__ void pack_sources(const float* __restrict__ ax, const float* __restri
         float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f);
         float4 r1 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < n) {
-            const float X = scale * ax[i], Y = scale * ay[i], Z = scale * az[i];
+            const float X = sign * ax[i], Y = sign * ay[i], Z = sign * az[i];
             r0 = make_float4(X, X, Y, Y);
             r1 = make_float4(Z, Z, wr[i], wi[i]);
         }
@@ -351,15 +413,12 @@ __global__ void pack_sources(const float* __restrict__ ax, const float* __restri
 
 // Segment descriptors: one thread per SEG sources.  A segment is flagged
 // when its real sources (index < n) have coordinates a_s = a_0 + (s - s0) * D
-// exactly (checked in double on the caller's unscaled coordinates, where these
-// products and sums are exact); the descriptor holds the scaled step
-// scale * D rounded once to float32.  The packed coordinates are
-// fl(scale * a_s), so A_0 + s * fl(scale * D) differs from them only by
-// rounding (fast mode's scale 2 pi breaks exact spacing of the packed values
-// themselves).  Sources at index >= n are zero-weight padding.
+// exactly, with the step D itself a float32 value (checked in double on the
+// caller's coordinates, where these products and sums are exact); the
+// descriptor holds sign * D.  Sources at index >= n are zero-weight padding.
 template <int SEG>
 __global__ void describe_segments(const float* __restrict__ ax, const float* __restrict__ ay,
-                                  const float* __restrict__ az, float scale, int64_t n, int64_t n_segments,
+                                  const float* __restrict__ az, float sign, int64_t n, int64_t n_segments,
                                   float4* __restrict__ desc, const uint32_t* skip) {
     if (skip != nullptr && *skip != 0u) return;
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < n_segments;
@@ -370,11 +429,11 @@ __global__ void describe_segments(const float* __restrict__ ax, const float* __r
         if (real >= 2) {
             const double x0 = ax[s0], y0 = ay[s0], z0 = az[s0];
             const double dx = (double)ax[s0 + 1] - x0, dy = (double)ay[s0 + 1] - y0, dz = (double)az[s0 + 1] - z0;
-            bool ok = true;
+            bool ok = (double)(float)dx == dx && (double)(float)dy == dy && (double)(float)dz == dz;
             for (int64_t s = 2; s < real && ok; ++s)
                 ok = (double)ax[s0 + s] == x0 + (double)s * dx && (double)ay[s0 + s] == y0 + (double)s * dy &&
                      (double)az[s0 + s] == z0 + (double)s * dz;
-            out = make_float4((float)(scale * dx), (float)(scale * dy), (float)(scale * dz), ok ? 1.f : 0.f);
+            out = make_float4(sign * (float)dx, sign * (float)dy, sign * (float)dz, ok ? 1.f : 0.f);
         }
         desc[g] = out;
     }
@@ -403,7 +462,8 @@ struct __align__(16) GatherSmem {
 // direct_group<MODE>() with fresh per-tile accumulators; each group's tile sums are
 // folded into the thread's running sums in shared memory.  In fast mode the
 // last NPOLY slots of a group take the FMA-pipe polynomial, the others the
-// MUFU pipe.
+// MUFU pipe; accurate mode takes the compensated phase and the accurate
+// polynomial on every pair.
 template <int MODE, int NPOLY>
 __device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, const float (*coord)[kThreads],
                                                 float (*run)[kThreads], int tid) {
@@ -429,14 +489,15 @@ __device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, 
             const float4 r1 = rec[2 * s + 1];  // A.z A.z w.re w.im
 #pragma unroll
             for (int v = 0; v < kDirectGroup; ++v) {
-                const float p = fmaf(r1.x, bz[v], fmaf(r0.z, by[v], r0.x * bx[v]));
                 float sn, cs;
                 if constexpr (MODE == kAccurate) {
-                    phasor_accurate(p, sn, cs);
-                } else if (v >= kDirectGroup - NPOLY) {
-                    phasor_poly(p, sn, cs);
+                    phasor_accurate(r0.x, r0.z, r1.x, bx[v], by[v], bz[v], sn, cs);
                 } else {
-                    phasor_mufu(p, sn, cs);
+                    const float p = fmaf(r1.x, bz[v], fmaf(r0.z, by[v], r0.x * bx[v]));
+                    if (v >= kDirectGroup - NPOLY)
+                        sincos2pi_poly<false>(p, sn, cs);
+                    else
+                        phasor_mufu(p, sn, cs);
                 }
                 gr[v] = fmaf(r1.z, cs, gr[v]);
                 gr[v] = fmaf(-r1.w, sn, gr[v]);
@@ -490,10 +551,15 @@ __host__ __device__ constexpr bool two_chain_negated(int v) { return ((v >> 1) &
 // Equal-spacing recurrence.  When a thread's kV consecutive targets satisfy
 // b_v = b_0 + v*d exactly, exp(i 2 pi a.b_v) = exp(i 2 pi a.b_0) * u^v with
 // u = exp(i 2 pi a.d).  Per source the thread evaluates two phasors (b_0 and
-// d, phases formed as packed pairs) and g_0 = w_s exp(i 2 pi a.b_0),
-// g_1 = g_0 u.  The real and imaginary parts of g_v = g_0 u^v each follow
-// g_{v+1} = 2 cos(theta_d) g_v - g_{v-1} (u + 1/u = 2 cos theta_d for
-// |u| = 1); its fp32 error grows at most like eps * v^2 / 2.  With the signs
+// d; in fast mode the phases are formed and reduced as packed pairs, in
+// accurate mode each by the compensated reduction) and g_0 = w_s exp(i 2 pi
+// a.b_0), g_1 = g_0 u.  The real and imaginary parts of g_v = g_0 u^v each
+// follow g_{v+1} = 2 cos(theta_d) g_v - g_{v-1} (u + 1/u = 2 cos theta_d for
+// |u| = 1); its fp32 error grows at most like eps * v^2 / 2.  The two-chain
+// form steps by 2 cos(2 theta_d), taken as 2 - 4 sin^2(theta_d): near
+// theta_d = 0, where the coefficient approaches 2 and its rounding decides
+// how far the chain's rotation drifts, this keeps the relative precision of
+// sin(theta_d) (4 cos^2 - 2 would carry 8 times the error of cos).  With the signs
 // s_v = (+, +, -, -, ...) the scaled terms e_v = s_v g_v obey
 // e_{v+1} = -+2 cos(theta_d) e_v + e_{v-1} (the coefficient alternating,
 // -2 cos first), so each target costs one packed FMA for the step and one
@@ -505,23 +571,31 @@ __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict
 #pragma unroll
     for (int v = 0; v < kV; ++v) acc[v] = 0ull;  // +0.0f in both halves
     const f2_t bx = f2_pack(x0, dx), by = f2_pack(y0, dy), bz = f2_pack(z0, dz);
+    const f2_t neg1 = f2_pack(-1.0f, -1.0f), two_pi = f2_pack(kTwoPi, kTwoPi);
     constexpr int kU = TWO ? kUnrollTwoChains : kUnrollOneChain;
 #pragma unroll kU
     for (int s = 0; s < kTile; ++s) {
         const float4 r0 = rec[2 * s];      // A.x A.x A.y A.y
         const float4 r1 = rec[2 * s + 1];  // A.z A.z w.re w.im
-        // (p0, pd) = A.b_0, A.d as one packed pair
-        const f2_t ph = f2_fma(f2_pack(r1.x, r1.y), bz,
-                               f2_fma(f2_pack(r0.z, r0.w), by, f2_mul(f2_pack(r0.x, r0.y), bx)));
-        float p0, pd;
-        f2_unpack(ph, p0, pd);
         float s0, c0, sw, cw;
         if constexpr (MODE == kAccurate) {
-            phasor_accurate(p0, s0, c0);
-            phasor_accurate(pd, sw, cw);
+            phasor_accurate(r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
+            phasor_step_accurate(r0.y, r0.w, r1.y, dx, dy, dz, sw, cw);
         } else {
-            phasor_mufu(p0, s0, c0);
-            phasor_mufu(pd, sw, cw);
+            // (p0, pd) = A.b_0, A.d as one packed pair, reduced to
+            // 2 pi (p - rint(p)) (the rounding on the XU pipe, which has room
+            // here: 4 sin/cos per 32 pairs)
+            const f2_t ph = f2_fma(f2_pack(r1.x, r1.y), bz,
+                                   f2_fma(f2_pack(r0.z, r0.w), by, f2_mul(f2_pack(r0.x, r0.y), bx)));
+            float p0, pd;
+            f2_unpack(ph, p0, pd);
+            const f2_t th = f2_mul(f2_fma(f2_pack(rintf(p0), rintf(pd)), neg1, ph), two_pi);
+            float th0, thd;
+            f2_unpack(th, th0, thd);
+            s0 = __sinf(th0);
+            c0 = __cosf(th0);
+            sw = __sinf(thd);
+            cw = __cosf(thd);
         }
         const float fr = fmaf(r1.z, c0, -r1.w * s0);  // g_0 = w_s * exp(i 2 pi a.b_0)
         const float fi = fmaf(r1.z, s0, r1.w * c0);
@@ -533,7 +607,10 @@ __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict
             const f2_t e0 = f2_pack(fr, fi), e1 = f2_pack(gr, gi);
             const f2_t e2n = f2_fma(f2_pack(-c2, -c2), e1, e0);  // -e_2
             const f2_t e3n = f2_fma(kpos, e2n, e1);              // -e_3
-            const float cc = fmaf(c2, c2, -2.0f);                 // 2 cos(2 theta_d)
+            // 2 cos(2 theta_d): accurate mode by two_cos_double; fast mode as
+            // 2 - 4 sin^2(theta_d) (the hardware sine keeps its precision near
+            // 0, where most steps of an image grid lie)
+            const float cc = MODE == kAccurate ? two_cos_double(sw, cw) : fmaf(-4.0f * sw, sw, 2.0f);
             const f2_t kposC = f2_pack(cc, cc), knegC = f2_pack(-cc, -cc);
             f2_t amA = e0, aA = e2n, amB = e1, aB = e3n;           // chains over even and odd targets
             acc[0] = f2_add(acc[0], e0);
@@ -572,9 +649,9 @@ __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict
 // Accurate mode, every lane of the warp with the same target spacing d: the
 // step phasor u_s = exp(i 2 pi a_s.d) is the same for all lanes, so lane l
 // evaluates it for sources 32k + l only and the others read it by shuffle.
-// Phases and sin/cos are those of accumulate_tile_strided (pd formed in the
-// same order), so the sums are bit-identical to it, with 1/32 of the
-// sincospif calls for u.
+// Phases and sin/cos are those of accumulate_tile_strided (the same
+// operations in the same order), so the sums are bit-identical to it, with
+// 1/32 of the sin/cos evaluations for u.
 __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* __restrict__ rec, float x0,
                                                                  float y0, float z0, float dx, float dy, float dz,
                                                                  int lane, f2_t (&acc)[kV]) {
@@ -587,14 +664,14 @@ __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* _
         {
             const float4 r0 = rec[2 * (s32 + lane)];
             const float4 r1 = rec[2 * (s32 + lane) + 1];
-            phasor_accurate(fmaf(r1.y, dz, fmaf(r0.w, dy, r0.y * dx)), su_l, cu_l);
+            phasor_step_accurate(r0.y, r0.w, r1.y, dx, dy, dz, su_l, cu_l);
         }
 #pragma unroll kUnrollSharedU
         for (int q = 0; q < 32; ++q) {
             const float4 r0 = rec[2 * (s32 + q)];      // A.x A.x A.y A.y
             const float4 r1 = rec[2 * (s32 + q) + 1];  // A.z A.z w.re w.im
             float s0, c0;
-            phasor_accurate(fmaf(r1.x, z0, fmaf(r0.z, y0, r0.x * x0)), s0, c0);
+            phasor_accurate(r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
             const float sw = __shfl_sync(0xffffffffu, su_l, q);
             const float cw = __shfl_sync(0xffffffffu, cu_l, q);
             const float fr = fmaf(r1.z, c0, -r1.w * s0);  // g_0 = w_s * exp(i 2 pi a.b_0)
@@ -606,7 +683,7 @@ __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* _
             const f2_t e0 = f2_pack(fr, fi), e1 = f2_pack(gr, gi);
             const f2_t e2n = f2_fma(f2_pack(-c2, -c2), e1, e0);  // -e_2
             const f2_t e3n = f2_fma(kpos, e2n, e1);              // -e_3
-            const float cc = fmaf(c2, c2, -2.0f);                 // 2 cos(2 theta_d)
+            const float cc = two_cos_double(sw, cw);              // 2 cos(2 theta_d)
             const f2_t kposC = f2_pack(cc, cc), knegC = f2_pack(-cc, -cc);
             f2_t amA = e0, aA = e2n, amB = e1, aB = e3n;           // chains over even and odd targets
             acc[0] = f2_add(acc[0], e0);
@@ -673,8 +750,8 @@ __device__ __forceinline__ bool equally_spaced(const float (&c)[kV], int n, floa
 // Source-side recurrence, for tiles whose every segment of kSegment sources
 // is equally spaced (a row of an image grid when the voxels are the sources,
 // as in the forward sum F rho).  For target b and segment sources
-// A_s = A_0 + s d: exp(i A_s.b) = e_0 u^s with e_0 = exp(i A_0.b) and
-// u = exp(i d.b).  Per (target, segment) one phasor, e_0, and per (target,
+// A_s = A_0 + s d: exp(i 2 pi A_s.b) = e_0 u^s with e_0 = exp(i 2 pi A_0.b)
+// and u = exp(i 2 pi d.b).  Per (target, segment) one phasor, e_0, and per (target,
 // run of segments with the same step) one more, u; the real and imaginary
 // parts of e_s follow e_{s+1} = 2 cos(d.b) e_s - e_{s-1} (error growth at most
 // eps * s^2 / 2 over the kSegment sources).  As in the target-side
@@ -705,7 +782,13 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
             Q[v] = 0ull;
         }
         // u = exp(i d.b) is evaluated only when a segment's step d differs
-        // from the previous segment's (on an image grid, once per tile)
+        // from the previous segment's (on an image grid, once per tile), from
+        // the phasor of half the step h: sin = 2 sin(h) cos(h), and
+        // cos = 1 - 2 sin^2(h) near d.b = 0 (fast mode: always), 2 cos^2(h) - 1
+        // near d.b = pi (accurate mode), which keeps the chain coefficient
+        // 2 cos(d.b) precise where the chain is most sensitive to it, as in
+        // the target-side recurrence; accurate mode takes the step from
+        // sincospif (see phasor_step_accurate)
         float cu[kSourceGroup], su[kSourceGroup];
         float4 d_prev = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
@@ -714,25 +797,29 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
             const float4 b1 = rec[2 * j * kSeg + 1];  // A_0.z A_0.z w.re w.im
             const float4 d = desc[j];
             if (j == 0 || d.x != d_prev.x || d.y != d_prev.y || d.z != d_prev.z) {  // uniform over the CTA
+                const float hx = 0.5f * d.x, hy = 0.5f * d.y, hz = 0.5f * d.z;
 #pragma unroll
                 for (int v = 0; v < kSourceGroup; ++v) {
-                    const float pd = fmaf(d.z, bz[v], fmaf(d.y, by[v], d.x * bx[v]));
-                    if constexpr (MODE == kAccurate)
-                        phasor_accurate(pd, su[v], cu[v]);
-                    else
-                        phasor_mufu(pd, su[v], cu[v]);
+                    float sh, ch;
+                    if constexpr (MODE == kAccurate) {
+                        phasor_step_accurate(hx, hy, hz, bx[v], by[v], bz[v], sh, ch);
+                        cu[v] = fabsf(sh) < fabsf(ch) ? fmaf(-2.0f * sh, sh, 1.0f) : fmaf(2.0f * ch, ch, -1.0f);
+                    } else {
+                        phasor_mufu(fmaf(hz, bz[v], fmaf(hy, by[v], hx * bx[v])), sh, ch);
+                        cu[v] = fmaf(-2.0f * sh, sh, 1.0f);
+                    }
+                    su[v] = (sh + sh) * ch;
                 }
                 d_prev = d;
             }
             f2_t fm[kSourceGroup], f[kSourceGroup], kpos[kSourceGroup], kneg[kSourceGroup];
 #pragma unroll
             for (int v = 0; v < kSourceGroup; ++v) {
-                const float p0 = fmaf(b1.x, bz[v], fmaf(b0.z, by[v], b0.x * bx[v]));
                 float s0, c0;
                 if constexpr (MODE == kAccurate)
-                    phasor_accurate(p0, s0, c0);
+                    phasor_accurate(b0.x, b0.z, b1.x, bx[v], by[v], bz[v], s0, c0);
                 else
-                    phasor_mufu(p0, s0, c0);
+                    phasor_mufu(fmaf(b1.x, bz[v], fmaf(b0.z, by[v], b0.x * bx[v])), s0, c0);
                 fm[v] = f2_pack(c0, s0);  // f_0 = e_0
                 f[v] = f2_pack(fmaf(c0, cu[v], -s0 * su[v]), fmaf(c0, su[v], s0 * cu[v]));  // f_1 = e_0 u
                 const float c2 = cu[v] + cu[v];
@@ -1047,13 +1134,13 @@ template <int MODE>
 __global__ void __launch_bounds__(kSplitThreads) split_gather_kernel(
     const float* __restrict__ tx, const float* __restrict__ ty, const float* __restrict__ tz, int64_t n_targets,
     const float* __restrict__ ax, const float* __restrict__ ay, const float* __restrict__ az,
-    const float* __restrict__ wr, const float* __restrict__ wi, float scale, int64_t n_sources, int64_t slice_len,
+    const float* __restrict__ wr, const float* __restrict__ wi, float sign, int64_t n_sources, int64_t slice_len,
     float* __restrict__ partial, float* __restrict__ out_r, float* __restrict__ out_i, uint32_t* status,
     int reset_status, const uint32_t* skip) {
     if (skip != nullptr && *skip != 0u) return;
     if (reset_status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0u;
-    // a chunk of sources as (A.x, A.y, A.z) with A = scale * a, rounded once
-    // as pack_sources rounds them, and their weights
+    // a chunk of sources as (A.x, A.y, A.z) with A = sign * a, as
+    // pack_sources stores them, and their weights
     __shared__ float4 rec[kSplitChunk];
     __shared__ float2 wrec[kSplitChunk];
     const int64_t t = (int64_t)blockIdx.x * kSplitThreads + threadIdx.x;
@@ -1067,7 +1154,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_gather_kernel(
         __syncthreads();  // the previous chunk is consumed
         for (int i = threadIdx.x; i < n; i += kSplitThreads) {
             const int64_t q = c0 + i;
-            rec[i] = make_float4(scale * ax[q], scale * ay[q], scale * az[q], 0.f);
+            rec[i] = make_float4(sign * ax[q], sign * ay[q], sign * az[q], 0.f);
             wrec[i] = make_float2(wr[q], wi[q]);
         }
         __syncthreads();
@@ -1075,12 +1162,11 @@ __global__ void __launch_bounds__(kSplitThreads) split_gather_kernel(
         for (int s = 0; s < n; ++s) {
             const float4 r = rec[s];
             const float2 w = wrec[s];
-            const float p = fmaf(r.z, bz, fmaf(r.y, by, r.x * bx));
             float sn, cs;
             if constexpr (MODE == kAccurate)
-                phasor_accurate(p, sn, cs);
+                phasor_accurate(r.x, r.y, r.z, bx, by, bz, sn, cs);
             else
-                phasor_mufu(p, sn, cs);
+                phasor_mufu(fmaf(r.z, bz, fmaf(r.y, by, r.x * bx)), sn, cs);
             ar = fmaf(w.x, cs, ar);
             ar = fmaf(-w.y, sn, ar);
             ai = fmaf(w.x, sn, ai);
