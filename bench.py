@@ -17,22 +17,22 @@ e2e        the same metric through the public API with pinned HOST buffers:
            pipelined client would, step k+1's inputs and step k's result
            cross the host link on two copy streams while step k computes.
 roofline   the gather kernel against its plain-ALU bound
-           SMs x clock x min(128 / n_fma, 16 / n_mufu, 128 / n_issue) pairs/s:
-           128 FP32 lanes, 16 MUFU lanes and 4 schedulers issuing one warp
-           instruction (32 lanes) per clock, per SM; n_fma, n_mufu and n_issue
-           are the algorithm's FP32 lane operations, MUFU operations and
-           instructions per pair.  Pair by pair (direct): 7 + 13/16,
-           2 * 15/16, 9 + 11/16 (k.x and the complex MAC; sin, cos on the
-           MUFU pipe for 15 of 16 pairs, an FMA-pipe polynomial for the 16th).
-           Equal-spacing recurrence on the benchmark's grid voxels, V = 32 targets per thread, packed f32x2 arithmetic:
-           per target one packed add and (from the third target on) one packed
-           three-term step (two chains, over even and odd targets), plus per
-           (thread, sample) the two phases (3 packed instructions),
-           D*exp(i theta_0) (4), its first step (4), 2 cos(theta_d) (1),
-           2 cos(2 theta_d) (1) and 4 MUFU -> n_fma = 4 - 4/V + 16/V,
-           n_mufu = 4/V, n_issue = 2 + 15/V.  Maximum SM clock.  The kernel's
-           duration comes from CUDA events recorded on its stream around the
-           gather and fix-up launches of every timed step.
+           SMs x clock x min(128 / n_fma, 16 / n_xu, 128 / n_issue) pairs/s:
+           128 FP32 lanes, a 16-lane pipe for the hardware sin/cos and the
+           rounding rintf, and 4 schedulers issuing one warp instruction (32
+           lanes) per clock, per SM; n_fma, n_xu and n_issue are the
+           algorithm's FP32 lane operations, 16-lane-pipe operations and
+           instructions per pair (per_pair_counts: every phase range-reduced
+           before its sin/cos, polar weights in the adjoint gather).  On the
+           benchmark's grid voxels the fast gather runs the equal-spacing
+           recurrence, V = 32 targets per thread, packed f32x2 arithmetic, two
+           chains: n_fma = 4 - 4/V + 19/V, n_xu = 6/V, n_issue = 2 + 19/V.
+           Maximum SM clock.  The kernel's duration comes from CUDA events
+           recorded on its stream around the gather and fix-up launches of
+           every timed step.
+secondary  the accurate mode evaluated pair by pair (the path of non-grid
+           voxels) on the same workload, two steps after the timed region,
+           with its own roofline (default line only; --no-secondary skips it).
 cpu_baseline  the fp64 CPU oracle on a bounded voxel sample of the same
            workload (test infrastructure; never used by the GPU path).
 
@@ -65,40 +65,66 @@ TARGETS_PER_THREAD = 32
 
 
 def per_pair_counts(path: str):
-    """(FP32 lane operations, MUFU operations, issued instructions) per pair of
-    the algorithm on `path` (all three count what the algorithm needs, not what
-    the compiler emits)."""
+    """(FP32 lane operations, 16-lane-pipe operations, issued instructions) per
+    pair of the algorithm on `path` (all three count what the algorithm needs,
+    not what the compiler emits; the 16-lane pipe runs the hardware sin/cos and
+    the rounding rintf).  Every phase is in cycles and range-reduced before
+    its sin/cos; the adjoint gathers' weights are polar {|w|, arg(w) / 2 pi},
+    so the weight's phase joins the pair's phase and the multiply-accumulate
+    is two real FMAs."""
+    V = TARGETS_PER_THREAD
     if path == "direct":
-        # k.x (1 FMUL + 2 FFMA) + complex MAC (4 FFMA); sin, cos on the MUFU
-        # pipe for 15 of every 16 pairs, and for the 16th the FMA-pipe
-        # polynomial (reduction 3, half-angle square 1, S and C 7, sin and
-        # cos 2: 13 lane operations)
+        # per pair: k.x + arg(w) (3 FMA-pipe operations), |w| (cos, sin) into
+        # the sums (2 FFMA); 15 of 16 pairs: t = p - rint(p) with the FMA-pipe
+        # rounding (3) and 2 pi t (1), sin and cos on the 16-lane pipe; the
+        # 16th pair: the fast polynomial (half-period reduction 3, u^2 1,
+        # sin 4, cos 4) and 2 sign flips on the integer pipe
         g = 16.0
-        return 7.0 + 13.0 / g, 2.0 * (g - 1) / g, 9.0 - 2.0 / g + 13.0 / g
+        return 5.0 + (4.0 * (g - 1) + 12.0) / g, 2.0 * (g - 1) / g, 5.0 + (6.0 * (g - 1) + 14.0) / g
+    if path == "direct-accurate":
+        # per pair: the compensated phase (3 FMUL, 3 rintf, 3 FFMA, 3 FADD
+        # with arg(w)), the accurate polynomial (half-period reduction 3, u^2
+        # 1, sin 6, cos 5) with 2 sign flips, |w| (cos, sin) into the sums (2)
+        return 26.0, 3.0, 31.0
     if path == "source":
         # source-side recurrence (the forward gather: segments of S = 32
-        # voxel sources), groups of G = 8 targets, packed f32x2: per pair one
-        # packed three-term step and two packed FMAs into P = sum w.re e and
-        # Q = sum w.im e (6 lane
-        # operations, 3 instructions); per (target, segment) the phase of e_0
-        # (3), e_1 = e_0 u (4), 2 cos (1), the signed pair of 2 cos (2) and
-        # 2 MUFU (the step phasor u once per run of segments with the same
-        # step: once per tile on an image grid, not counted); per (source,
-        # group) one shared-memory load and the two signed weight pairs (4).
+        # voxel sources, Cartesian weights), groups of G = 8 targets, packed
+        # f32x2: per pair one packed three-term step and two packed FMAs into
+        # P = sum w.re e and Q = sum w.im e (6 lane operations, 3
+        # instructions); per (target, segment) the phase of e_0 (3), its
+        # reduction and 2 pi t (4), e_1 = e_0 u (4), 2 cos (1), the signed
+        # pair of 2 cos (2) and 2 sin/cos (the step phasor u once per run of
+        # segments with the same step: once per tile on an image grid, not
+        # counted); per (source, group) one shared-memory load and the two
+        # signed weight pairs (4).
         S, G = 32.0, 8.0
-        return 6.0 + 10.0 / S, 2.0 / S, 3.0 + 12.0 / S + 5.0 / G
-    # recurrence, V targets per thread, as two chains (even and odd targets).
-    # Per (thread, sample): the two phases as 3 packed instructions (6 lane
-    # operations), g_0 = D exp(i theta_0) (4), g_1 = g_0 u (4), 2 cos(theta_d)
-    # (1), 2 cos(2 theta_d) (1), 4 MUFU.  Per target: one packed add into its
+        return 6.0 + 14.0 / S, 2.0 / S, 3.0 + 16.0 / S + 5.0 / G
+    if path == "recurrence-accurate":
+        # the two-chain recurrence of accurate mode with the step phasor
+        # shared by the warp: per (thread, sample) the compensated phase of
+        # the anchor (9 FMA-pipe operations, 3 rintf), the accurate
+        # polynomial (15, 2 sign flips), g_0 = |w| (cos, sin) (2), g_1 (4),
+        # 2 cos (1), the coefficient 2 cos 2 theta chosen from sin or cos (5),
+        # the first two steps (4 lanes), 2 shuffles, and 1/32 of the step
+        # phasor (its compensated phase and sincospif, about 47 operations);
+        # per target the packed add and step (4 lanes, 2 instructions)
+        lanes = 4.0 - 4.0 / V + (9 + 15 + 2 + 4 + 1 + 5 + 4 + 47.0 / 32) / V
+        xu = (3.0 + 3.0 / 32) / V
+        issue = 2.0 + (-2 + 12 + 17 + 2 + 4 + 1 + 5 + 2 + 2 + 50.0 / 32) / V
+        return lanes, xu, issue
+    # recurrence (fast mode), V targets per thread, as two chains (even and
+    # odd targets).  Per (thread, sample): the two phases as 3 packed
+    # instructions (6 lane operations), + arg(w) (1), the two reductions
+    # (2 rintf, 2 FADD) and 2 pi t as one packed multiply (2 lanes),
+    # g_0 = |w| (cos, sin) (2), g_1 = g_0 u (4), 2 cos(theta_d) (1),
+    # 2 cos(2 theta_d) (1), 4 sin/cos.  Per target: one packed add into its
     # accumulator (2 lane operations), and from the third target on one
     # packed three-term step (2 lane operations; the steps to targets 2 and 3
     # use 2 cos(theta_d), the rest 2 cos(2 theta_d)).
-    V = TARGETS_PER_THREAD
-    lanes = 4.0 - 4.0 / V + 16.0 / V
-    mufu = 4.0 / V
-    issue = (2.0 * V - 2.0 + 3.0 + 4.0 + 4.0 + 1.0 + 1.0 + 4.0) / V
-    return lanes, mufu, issue
+    lanes = 4.0 - 4.0 / V + 19.0 / V
+    xu = 6.0 / V
+    issue = (2.0 * V - 2.0 + 3.0 + 1.0 + 2.0 + 2.0 + 1.0 + 4.0 + 2.0 + 4.0 + 1.0 + 1.0) / V
+    return lanes, xu, issue
 
 
 WORKLOAD_NAMES = {
@@ -120,6 +146,8 @@ def parse():
     ap.add_argument("--mode", choices=["fast", "accurate", "fast-direct", "accurate-direct"], default="fast")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the secondary accurate pair-by-pair measurement of the default line")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--ladder", action="store_true",
                     help="time the case study's optimisation ladder (include/fhd_ladder.h) next to the library "
@@ -391,9 +419,11 @@ def run_ours(args, world, rank, local):
     fhd.load()
     mode = {"fast": fhd.MODE_FAST, "accurate": fhd.MODE_ACCURATE, "fast-direct": fhd.MODE_FAST_DIRECT,
             "accurate-direct": fhd.MODE_ACCURATE_DIRECT}[args.mode]
-    # The benchmark voxels are power-of-two grids: every thread's 8 consecutive
-    # voxels are exactly equally spaced, so the recurrence runs unless disabled.
-    path = "direct" if args.mode.endswith("direct") else "recurrence"
+    # The benchmark voxels are power-of-two grids: every thread's 32
+    # consecutive voxels are exactly equally spaced, so the recurrence runs
+    # unless disabled.
+    path = {"fast": "recurrence", "accurate": "recurrence-accurate", "fast-direct": "direct",
+            "accurate-direct": "direct-accurate"}[args.mode]
     p = load_workload(args.workload)
     fhf = p.op == "fhf"
     if fhf:  # F^H F rho: the forward gather (voxel sources) then the adjoint gather
@@ -409,7 +439,7 @@ def run_ours(args, world, rank, local):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     input_bytes = sum(v.numel() * 4 for v in d.values())
 
-    def step(e0=None, e1=None, dd=None, out=None):
+    def step(e0=None, e1=None, dd=None, out=None, mode=mode):
         dd = d if dd is None else dd
         rr, ri = (rho_r, rho_i) if out is None else out
         if fhf:
@@ -588,6 +618,44 @@ def run_ours(args, world, rank, local):
     }
     if clk.get("sm_mhz"):
         roof["frac_at_sampled_clock"] = achieved / peak_pairs_per_s(sms, clk["sm_mhz"], path)
+    if fhf and not args.mode.startswith("fast"):
+        roof["peak_basis"] += " (the fast mode's operation counts: an upper bound for accurate mode)"
+
+    # ---- secondary: the accurate pair-by-pair path on the same workload (the
+    # path a caller with non-grid voxels takes in accurate mode), a few steps
+    secondary = None
+    if not fhf and args.mode == "fast" and not args.no_secondary:
+        acc_mode = fhd.MODE_ACCURATE_DIRECT
+        step(mode=acc_mode)
+        torch.cuda.synchronize()
+        sec = []
+        for _ in range(2):
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for e in (a0, a1, g0, g1):
+                e.record(stream)
+            torch.cuda.synchronize()
+            a0.record(stream)
+            step(g0, g1, mode=acc_mode)
+            a1.record(stream)
+            torch.cuda.synchronize()
+            sec.append((a0.elapsed_time(a1), g0.elapsed_time(g1)))
+        s_ms = sum(x[0] for x in sec) / len(sec)
+        s_gather = sum(x[1] for x in sec) / len(sec)
+        s_peak = peak_pairs_per_s(sms, max_mhz, "direct-accurate")
+        s_ach = pairs / (s_gather * 1e-3)
+        nf, nx, ni = per_pair_counts("direct-accurate")
+        secondary = {
+            "mode": "accurate-direct", "value": pairs / (s_ms * 1e-3), "unit": "pairs/s", "ms_per_step": s_ms,
+            "steps": len(sec), "warmup": 1,
+            "roofline": {"bound": "alu", "achieved": FLOP_PER_PAIR * s_ach / 1e12,
+                         "peak": FLOP_PER_PAIR * s_peak / 1e12, "unit": "TFLOP/s", "frac": s_ach / s_peak,
+                         "kernel_ms": s_gather, "path": "direct-accurate",
+                         "peak_basis": f"{sms} SMs x {max_mhz:.0f} MHz x min({FMA_LANES_PER_SM}/{nf:g}, "
+                                       f"{MUFU_LANES_PER_SM}/{nx:g}, {ISSUE_PER_SM}/{ni:g}) pairs/clk x "
+                                       f"{FLOP_PER_PAIR} flop/pair"},
+            "note": "accurate mode evaluated pair by pair (FHD_MODE_ACCURATE_DIRECT): the path of non-grid voxels",
+        }
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -624,6 +692,7 @@ def run_ours(args, world, rank, local):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "roofline": roof,
+        "secondary": secondary,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches * args.steps,

@@ -42,10 +42,10 @@ cudaError_t max_ctas(int device, fhd_mode mode, int* out) {
     const size_t smem = sizeof(GatherSmem);
     if (fast)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, gather_kernel<kFast, kFastPolySlots, segment_len<kFast>()>, kCtaThreads, smem);
+            &per_sm, gather_kernel<kFast, kFastPolySlots, segment_len<kFast>(), kPolarAdjoint>, kCtaThreads, smem);
     else
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, gather_kernel<kAccurate, 0, segment_len<kAccurate>()>, kCtaThreads, smem);
+            &per_sm, gather_kernel<kAccurate, 0, segment_len<kAccurate>(), kPolarAdjoint>, kCtaThreads, smem);
     if (e != cudaSuccess) return e;
     per_sm = std::min(std::max(per_sm, 1), kMinCtasPerSm);
     *out = sms * per_sm;
@@ -204,9 +204,11 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
         return FHD_OK;
     }
 
+    // polar weights in the adjoint gather (see pack_sources)
+    const bool polar = kPolarAdjoint && g.sign > 0.f;
     const int pack_grid = (int)std::min<int64_t>(ceil_div(padded, 256), (int64_t)sms * 8);
-    pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, sign, g.n_sources, padded,
-                                                packed, status, first_pass ? 1 : 0, skip);
+    pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, sign, polar ? 1 : 0, g.n_sources,
+                                                padded, packed, status, first_pass ? 1 : 0, skip);
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
 
     float4* desc = reinterpret_cast<float4*>(ws + L.desc);
@@ -243,18 +245,24 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     const size_t smem = sizeof(GatherSmem);
     if (fast_mode(mode)) {
         if (g.sign < 0.f) {
-            constexpr auto k = gather_kernel<kFast, kFastPolySlots, kSegmentAccurate>;
+            constexpr auto k = gather_kernel<kFast, kFastPolySlots, kSegmentAccurate, false>;
             cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             k<<<sch.ctas, kCtaThreads, smem, stream>>>(a);
         } else {
-            constexpr auto k = gather_kernel<kFast, kFastPolySlots, kSegment>;
+            constexpr auto k = gather_kernel<kFast, kFastPolySlots, kSegment, kPolarAdjoint>;
             cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             k<<<sch.ctas, kCtaThreads, smem, stream>>>(a);
         }
     } else {
-        constexpr auto k = gather_kernel<kAccurate, 0, kSegmentAccurate>;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<sch.ctas, kCtaThreads, smem, stream>>>(a);
+        if (g.sign < 0.f) {
+            constexpr auto k = gather_kernel<kAccurate, 0, kSegmentAccurate, false>;
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            k<<<sch.ctas, kCtaThreads, smem, stream>>>(a);
+        } else {
+            constexpr auto k = gather_kernel<kAccurate, 0, kSegmentAccurate, kPolarAdjoint>;
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            k<<<sch.ctas, kCtaThreads, smem, stream>>>(a);
+        }
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
     if (sch.ctas > 1) {

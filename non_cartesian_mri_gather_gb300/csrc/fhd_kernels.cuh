@@ -81,6 +81,9 @@ namespace fhd {
 #ifndef FHD_UNROLL
 #define FHD_UNROLL 4
 #endif
+#ifndef FHD_POLAR_WEIGHTS
+#define FHD_POLAR_WEIGHTS 1
+#endif
 
 constexpr int kThreads = FHD_THREADS;    // consumer threads per CTA
 constexpr int kWarps = kThreads / 32;    // consumer warps
@@ -101,12 +104,16 @@ static_assert(kTile % kSegment == 0, "tiles hold whole segments");
 constexpr int kCtaThreads = kThreads + 32;  // + one producer warp
 constexpr int kMinCtasPerSm = FHD_MIN_CTAS_PER_SM;
 constexpr int kUnroll = FHD_UNROLL;      // sources per unrolled inner-loop step
-constexpr int kUnrollSharedU = 8;        // the same in the accurate warp-shared-phasor loop (measured best)
+constexpr int kUnrollSharedU = 12;       // the same in the accurate warp-shared-phasor loop (measured best)
 // and in the target-side recurrence's sample loop (measured best): two
 // chains (the fast adjoint and the accurate kernels), one chain (the fast
 // forward kernel)
-constexpr int kUnrollTwoChains = 5;
+constexpr int kUnrollTwoChains = 6;
 constexpr int kUnrollOneChain = 3;
+// The adjoint gathers store each weight in polar form, {|w|, arg(w) / 2 pi}
+// (see pack_sources); the forward gathers, whose voxel weights feed the
+// source-side recurrence's real-weighted sums, keep {w.re, w.im}.
+constexpr bool kPolarAdjoint = FHD_POLAR_WEIGHTS != 0;
 static_assert(kThreads % 32 == 0 && kTile % 2 == 0 && kStages >= 2, "bad launch shape");
 
 // status word bits
@@ -356,6 +363,14 @@ __device__ __forceinline__ void phasor_accurate(float ax, float ay, float az, fl
     sincos2pi_poly<true>(phase_accurate(ax, ay, az, bx, by, bz), s, c);
 }
 
+// The same for 2 pi (a.b + phi), |phi| <= 1/2: the phase of a polar weight
+// (see pack_sources) added to the reduced phase, one more rounding of a value
+// below 2.5.
+__device__ __forceinline__ void phasor_accurate_off(float phi, float ax, float ay, float az, float bx, float by,
+                                                    float bz, float& s, float& c) {
+    sincos2pi_poly<true>(phase_accurate(ax, ay, az, bx, by, bz) + phi, s, c);
+}
+
 // Accurate mode, the step phasor of a recurrence: sin, cos of 2 pi a.b with
 // sincospif on the compensated phase.  A recurrence rotates by the step's
 // angle once per target, so a relative error of that angle grows with the
@@ -385,14 +400,19 @@ __device__ __forceinline__ float two_cos_double(float s, float c) {
 // (exact; sign is -1 for the forward sum, whose sources are the voxels, and +1
 // for the adjoint sum; phases are in cycles in both modes): each coordinate
 // twice, so one 16-byte load gives (A.x, A.x, A.y, A.y) as the packed pairs
-// the recurrence multiplies by (x0, dx) and (y0, dy).
+// the recurrence multiplies by (x0, dx) and (y0, dy).  With `polar` the
+// weight is stored as {|w|, phi}, phi = arg(w) / 2 pi in [-1/2, 1/2] cycles
+// (both from double precision, each rounded once): w exp(i 2 pi a.b) =
+// |w| exp(i 2 pi (a.b + phi)), so phi joins the phase (the first product of
+// the phase becomes an FMA) and the complex multiply-accumulate of a pair
+// becomes two real ones.
 // Records n..n_padded-1 are zero (weight 0, so they add exactly 0).
 // With `reset_status`, block 0 thread 0 also clears the status word (stream
 // order puts this before the gather kernel); the second pass of F^H F rho
 // keeps the word so a timeout of the first pass stays visible.
 __global__ void pack_sources(const float* __restrict__ ax, const float* __restrict__ ay,
                              const float* __restrict__ az, const float* __restrict__ wr,
-                             const float* __restrict__ wi, float sign, int64_t n, int64_t n_padded,
+                             const float* __restrict__ wi, float sign, int polar, int64_t n, int64_t n_padded,
                              float4* __restrict__ out, uint32_t* status, int reset_status,
                              const uint32_t* skip) {
     if (skip != nullptr && *skip != 0u) return;
@@ -404,7 +424,12 @@ __global__ void pack_sources(const float* __restrict__ ax, const float* __restri
         if (i < n) {
             const float X = sign * ax[i], Y = sign * ay[i], Z = sign * az[i];
             r0 = make_float4(X, X, Y, Y);
-            r1 = make_float4(Z, Z, wr[i], wi[i]);
+            if (polar) {
+                const double re = wr[i], im = wi[i];
+                r1 = make_float4(Z, Z, (float)hypot(re, im), (float)(atan2(im, re) * 0.15915494309189533577));
+            } else {
+                r1 = make_float4(Z, Z, wr[i], wi[i]);
+            }
         }
         out[2 * i] = r0;
         out[2 * i + 1] = r1;
@@ -464,7 +489,7 @@ struct __align__(16) GatherSmem {
 // last NPOLY slots of a group take the FMA-pipe polynomial, the others the
 // MUFU pipe; accurate mode takes the compensated phase and the accurate
 // polynomial on every pair.
-template <int MODE, int NPOLY>
+template <int MODE, int NPOLY, bool POLAR>
 __device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, const float (*coord)[kThreads],
                                                 float (*run)[kThreads], int tid) {
     constexpr int kDirectGroup = direct_group<MODE>();
@@ -491,18 +516,26 @@ __device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, 
             for (int v = 0; v < kDirectGroup; ++v) {
                 float sn, cs;
                 if constexpr (MODE == kAccurate) {
-                    phasor_accurate(r0.x, r0.z, r1.x, bx[v], by[v], bz[v], sn, cs);
+                    if constexpr (POLAR)
+                        phasor_accurate_off(r1.w, r0.x, r0.z, r1.x, bx[v], by[v], bz[v], sn, cs);
+                    else
+                        phasor_accurate(r0.x, r0.z, r1.x, bx[v], by[v], bz[v], sn, cs);
                 } else {
-                    const float p = fmaf(r1.x, bz[v], fmaf(r0.z, by[v], r0.x * bx[v]));
+                    const float p = fmaf(r1.x, bz[v], fmaf(r0.z, by[v], POLAR ? fmaf(r0.x, bx[v], r1.w) : r0.x * bx[v]));
                     if (v >= kDirectGroup - NPOLY)
                         sincos2pi_poly<false>(p, sn, cs);
                     else
                         phasor_mufu(p, sn, cs);
                 }
-                gr[v] = fmaf(r1.z, cs, gr[v]);
-                gr[v] = fmaf(-r1.w, sn, gr[v]);
-                gi[v] = fmaf(r1.z, sn, gi[v]);
-                gi[v] = fmaf(r1.w, cs, gi[v]);
+                if constexpr (POLAR) {  // |w| (cos, sin) of the phase with arg(w) in it
+                    gr[v] = fmaf(r1.z, cs, gr[v]);
+                    gi[v] = fmaf(r1.z, sn, gi[v]);
+                } else {
+                    gr[v] = fmaf(r1.z, cs, gr[v]);
+                    gr[v] = fmaf(-r1.w, sn, gr[v]);
+                    gi[v] = fmaf(r1.z, sn, gi[v]);
+                    gi[v] = fmaf(r1.w, cs, gi[v]);
+                }
             }
         }
 #pragma unroll
@@ -556,22 +589,20 @@ __host__ __device__ constexpr bool two_chain_negated(int v) { return ((v >> 1) &
 // a.b_0), g_1 = g_0 u.  The real and imaginary parts of g_v = g_0 u^v each
 // follow g_{v+1} = 2 cos(theta_d) g_v - g_{v-1} (u + 1/u = 2 cos theta_d for
 // |u| = 1); its fp32 error grows at most like eps * v^2 / 2.  The two-chain
-// form steps by 2 cos(2 theta_d), taken as 2 - 4 sin^2(theta_d): near
-// theta_d = 0, where the coefficient approaches 2 and its rounding decides
-// how far the chain's rotation drifts, this keeps the relative precision of
-// sin(theta_d) (4 cos^2 - 2 would carry 8 times the error of cos).  With the signs
+// form steps by 2 cos(2 theta_d) (see two_cos_double for accurate mode).
+// With the signs
 // s_v = (+, +, -, -, ...) the scaled terms e_v = s_v g_v obey
 // e_{v+1} = -+2 cos(theta_d) e_v + e_{v-1} (the coefficient alternating,
 // -2 cos first), so each target costs one packed FMA for the step and one
 // packed add into its accumulator, which holds s_v times the sum.  Voxels of a
 // regular image grid, and samples along a radial spoke, are equally spaced.
-template <int MODE, bool TWO>
+template <int MODE, bool TWO, bool POLAR>
 __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict__ rec, float x0, float y0,
                                                         float z0, float dx, float dy, float dz, f2_t (&acc)[kV]) {
 #pragma unroll
     for (int v = 0; v < kV; ++v) acc[v] = 0ull;  // +0.0f in both halves
     const f2_t bx = f2_pack(x0, dx), by = f2_pack(y0, dy), bz = f2_pack(z0, dz);
-    const f2_t neg1 = f2_pack(-1.0f, -1.0f), two_pi = f2_pack(kTwoPi, kTwoPi);
+    const f2_t two_pi = f2_pack(kTwoPi, kTwoPi);
     constexpr int kU = TWO ? kUnrollTwoChains : kUnrollOneChain;
 #pragma unroll kU
     for (int s = 0; s < kTile; ++s) {
@@ -579,17 +610,22 @@ __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict
         const float4 r1 = rec[2 * s + 1];  // A.z A.z w.re w.im
         float s0, c0, sw, cw;
         if constexpr (MODE == kAccurate) {
-            phasor_accurate(r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
+            if constexpr (POLAR)
+                phasor_accurate_off(r1.w, r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
+            else
+                phasor_accurate(r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
             phasor_step_accurate(r0.y, r0.w, r1.y, dx, dy, dz, sw, cw);
         } else {
             // (p0, pd) = A.b_0, A.d as one packed pair, reduced to
             // 2 pi (p - rint(p)) (the rounding on the XU pipe, which has room
-            // here: 4 sin/cos per 32 pairs)
+            // here: 4 sin/cos per 32 pairs; reducing each half on its own
+            // before the packed multiply measured fastest)
             const f2_t ph = f2_fma(f2_pack(r1.x, r1.y), bz,
                                    f2_fma(f2_pack(r0.z, r0.w), by, f2_mul(f2_pack(r0.x, r0.y), bx)));
             float p0, pd;
             f2_unpack(ph, p0, pd);
-            const f2_t th = f2_mul(f2_fma(f2_pack(rintf(p0), rintf(pd)), neg1, ph), two_pi);
+            if constexpr (POLAR) p0 += r1.w;  // the weight's phase (measured faster than in the packed FMA)
+            const f2_t th = f2_mul(f2_pack(p0 - rintf(p0), pd - rintf(pd)), two_pi);
             float th0, thd;
             f2_unpack(th, th0, thd);
             s0 = __sinf(th0);
@@ -597,8 +633,9 @@ __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict
             sw = __sinf(thd);
             cw = __cosf(thd);
         }
-        const float fr = fmaf(r1.z, c0, -r1.w * s0);  // g_0 = w_s * exp(i 2 pi a.b_0)
-        const float fi = fmaf(r1.z, s0, r1.w * c0);
+        // g_0 = w_s * exp(i 2 pi a.b_0)
+        const float fr = POLAR ? r1.z * c0 : fmaf(r1.z, c0, -r1.w * s0);
+        const float fi = POLAR ? r1.z * s0 : fmaf(r1.z, s0, r1.w * c0);
         const float gr = fmaf(fr, cw, -fi * sw);      // g_1 = g_0 u
         const float gi = fmaf(fr, sw, fi * cw);
         if constexpr (TWO) {
@@ -608,9 +645,10 @@ __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict
             const f2_t e2n = f2_fma(f2_pack(-c2, -c2), e1, e0);  // -e_2
             const f2_t e3n = f2_fma(kpos, e2n, e1);              // -e_3
             // 2 cos(2 theta_d): accurate mode by two_cos_double; fast mode as
-            // 2 - 4 sin^2(theta_d) (the hardware sine keeps its precision near
-            // 0, where most steps of an image grid lie)
-            const float cc = MODE == kAccurate ? two_cos_double(sw, cw) : fmaf(-4.0f * sw, sw, 2.0f);
+            // (2 cos theta_d)^2 - 2, one operation (its error, 8 times that of
+            // the hardware cosine, stays two orders below the fast tolerance;
+            // the precise forms measured 3 % slower here)
+            const float cc = MODE == kAccurate ? two_cos_double(sw, cw) : fmaf(c2, c2, -2.0f);
             const f2_t kposC = f2_pack(cc, cc), knegC = f2_pack(-cc, -cc);
             f2_t amA = e0, aA = e2n, amB = e1, aB = e3n;           // chains over even and odd targets
             acc[0] = f2_add(acc[0], e0);
@@ -652,6 +690,7 @@ __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict
 // Phases and sin/cos are those of accumulate_tile_strided (the same
 // operations in the same order), so the sums are bit-identical to it, with
 // 1/32 of the sin/cos evaluations for u.
+template <bool POLAR>
 __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* __restrict__ rec, float x0,
                                                                  float y0, float z0, float dx, float dy, float dz,
                                                                  int lane, f2_t (&acc)[kV]) {
@@ -671,11 +710,15 @@ __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* _
             const float4 r0 = rec[2 * (s32 + q)];      // A.x A.x A.y A.y
             const float4 r1 = rec[2 * (s32 + q) + 1];  // A.z A.z w.re w.im
             float s0, c0;
-            phasor_accurate(r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
+            if constexpr (POLAR)
+                phasor_accurate_off(r1.w, r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
+            else
+                phasor_accurate(r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
             const float sw = __shfl_sync(0xffffffffu, su_l, q);
             const float cw = __shfl_sync(0xffffffffu, cu_l, q);
-            const float fr = fmaf(r1.z, c0, -r1.w * s0);  // g_0 = w_s * exp(i 2 pi a.b_0)
-            const float fi = fmaf(r1.z, s0, r1.w * c0);
+            // g_0 = w_s * exp(i 2 pi a.b_0)
+            const float fr = POLAR ? r1.z * c0 : fmaf(r1.z, c0, -r1.w * s0);
+            const float fi = POLAR ? r1.z * s0 : fmaf(r1.z, s0, r1.w * c0);
             const float gr = fmaf(fr, cw, -fi * sw);      // g_1 = g_0 u
             const float gi = fmaf(fr, sw, fi * cw);
             const float c2 = cw + cw;
@@ -707,15 +750,15 @@ __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* _
 
 // One staged tile on the target-side recurrence, folded into the thread's
 // running sums (the signs of the stored terms undone here).
-template <int MODE, bool TWO>
+template <int MODE, bool TWO, bool POLAR>
 __device__ __forceinline__ void strided_tile(const float4* __restrict__ rec, float x0, float y0, float z0,
                                              float dx, float dy, float dz, int lane, bool shared_u,
                                              float (*run)[kThreads], int tid) {
     f2_t acc[kV];
     if (MODE == kAccurate && shared_u)
-        accumulate_tile_strided_shared_u(rec, x0, y0, z0, dx, dy, dz, lane, acc);
+        accumulate_tile_strided_shared_u<POLAR>(rec, x0, y0, z0, dx, dy, dz, lane, acc);
     else
-        accumulate_tile_strided<MODE, TWO>(rec, x0, y0, z0, dx, dy, dz, acc);
+        accumulate_tile_strided<MODE, TWO, POLAR>(rec, x0, y0, z0, dx, dy, dz, acc);
 #pragma unroll
     for (int v = 0; v < kV; ++v) {
         float re, im;
@@ -763,7 +806,27 @@ __device__ __forceinline__ bool equally_spaced(const float (&c)[kV], int n, floa
 // sum w_s e_s = (P.re - Q.im) + i (P.im + Q.re) at the end: per pair three
 // packed FMAs.  Targets go in groups of kSourceGroup; each group's tile sums
 // are folded straight into the thread's running sums.
-template <int MODE, int SEG>
+// A record's weight {w.re, w.im}; from polar records {|w|, phi}, |w| times
+// (cos, sin)(2 pi phi), |phi| <= 1/2 (fast mode: the hardware sin/cos of
+// 2 pi phi in [-pi, pi]; accurate mode: the accurate polynomial).
+template <int MODE, bool POLAR>
+__device__ __forceinline__ float2 record_weight(float a, float b) {
+    if constexpr (!POLAR) {
+        return make_float2(a, b);
+    } else {
+        float sn, cs;
+        if constexpr (MODE == kAccurate) {
+            sincos2pi_poly<true>(b, sn, cs);
+        } else {
+            const float th = kTwoPi * b;
+            sn = __sinf(th);
+            cs = __cosf(th);
+        }
+        return make_float2(a * cs, a * sn);
+    }
+}
+
+template <int MODE, int SEG, bool POLAR>
 __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __restrict__ rec,
                                                             const float4* __restrict__ desc,
                                                             const float (*coord)[kThreads], float (*run)[kThreads],
@@ -827,7 +890,8 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
                 kneg[v] = f2_pack(-c2, -c2);
             }
             {  // source 0 (sign +) takes f_0
-                const f2_t wr = f2_pack(b1.z, b1.z), wi = f2_pack(b1.w, b1.w);
+                const float2 w0 = record_weight<MODE, POLAR>(b1.z, b1.w);
+                const f2_t wr = f2_pack(w0.x, w0.x), wi = f2_pack(w0.y, w0.y);
 #pragma unroll
                 for (int v = 0; v < kSourceGroup; ++v) {
                     P[v] = f2_fma(wr, fm[v], P[v]);
@@ -836,9 +900,10 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
             }
 #pragma unroll
             for (int s = 1; s < kSeg; ++s) {
-                const float4 w = rec[2 * (j * kSeg + s) + 1];  // w.re, w.im in .z, .w
+                const float4 r = rec[2 * (j * kSeg + s) + 1];  // the weight in .z, .w
+                const float2 w = record_weight<MODE, POLAR>(r.z, r.w);
                 const float sg = strided_negated(s) ? -1.f : 1.f;   // s_s, folded into the weight
-                const f2_t wr = f2_pack(sg * w.z, sg * w.z), wi = f2_pack(sg * w.w, sg * w.w);
+                const f2_t wr = f2_pack(sg * w.x, sg * w.x), wi = f2_pack(sg * w.y, sg * w.y);
 #pragma unroll
                 for (int v = 0; v < kSourceGroup; ++v) {
                     P[v] = f2_fma(wr, f[v], P[v]);
@@ -868,25 +933,27 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
 // into it: measured on the 256^3 x 100000 grid, the accurate kernel runs its
 // recurrence fastest with these two paths called out of line, the fast kernel
 // with everything inlined.
-template <int MODE, int NPOLY>
+template <int MODE, int NPOLY, bool POLAR>
 __device__ __noinline__ void accumulate_tile_ool(const float4* __restrict__ rec, const float (*coord)[kThreads],
                                                  float (*run)[kThreads], int tid) {
-    accumulate_tile<MODE, NPOLY>(rec, coord, run, tid);
+    accumulate_tile<MODE, NPOLY, POLAR>(rec, coord, run, tid);
 }
-template <int MODE, int SEG>
+template <int MODE, int SEG, bool POLAR>
 __device__ __noinline__ void accumulate_tile_src_strided_ool(const float4* __restrict__ rec,
                                                              const float4* __restrict__ desc,
                                                              const float (*coord)[kThreads],
                                                              float (*run)[kThreads], int tid) {
-    accumulate_tile_src_strided<MODE, SEG>(rec, desc, coord, run, tid);
+    accumulate_tile_src_strided<MODE, SEG, POLAR>(rec, desc, coord, run, tid);
 }
 
 // MODE: kAccurate or kFast.  NPOLY (fast mode only): how many of the kV
 // register slots evaluate sin/cos with the FMA-pipe polynomial instead of the
 // MUFU pipe; it sets the split between the two pipes.  SEG: the source segment
 // length of the descriptors (segment_len<MODE>() for the adjoint gather,
-// kSegmentAccurate for the forward gather, each its own instantiation).
-template <int MODE, int NPOLY, int SEG>
+// kSegmentAccurate for the forward gather).  POLAR: the records hold polar
+// weights (the adjoint gather; see pack_sources).  Each combination in use is
+// its own instantiation.
+template <int MODE, int NPOLY, int SEG, bool POLAR>
 __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(const GatherArgs args) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // The target-side recurrence runs as two chains (even and odd targets),
@@ -1008,13 +1075,13 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
         const float4* rec = &sm.ring[st][0];
         if (strided) {
             if constexpr (MODE == kFast) {
-                strided_tile<MODE, kTwoChains>(rec, x0, y0, z0, sx, sy, sz, lane, shared_u, sm.run, tid);
+                strided_tile<MODE, kTwoChains, POLAR>(rec, x0, y0, z0, sx, sy, sz, lane, shared_u, sm.run, tid);
             } else {
                 f2_t acc[kV];
                 if (shared_u)
-                    accumulate_tile_strided_shared_u(rec, x0, y0, z0, sx, sy, sz, lane, acc);
+                    accumulate_tile_strided_shared_u<POLAR>(rec, x0, y0, z0, sx, sy, sz, lane, acc);
                 else
-                    accumulate_tile_strided<MODE, kTwoChains>(rec, x0, y0, z0, sx, sy, sz, acc);
+                    accumulate_tile_strided<MODE, kTwoChains, POLAR>(rec, x0, y0, z0, sx, sy, sz, acc);
 #pragma unroll
                 for (int v = 0; v < kV; ++v) {
                     float re, im;
@@ -1035,14 +1102,14 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
                 src_strided = src_strided && sm.desc[st][q].w != 0.f;
             if (src_strided) {
                 if constexpr (MODE == kFast)
-                    accumulate_tile_src_strided<MODE, SEG>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
+                    accumulate_tile_src_strided<MODE, SEG, POLAR>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
                 else
-                    accumulate_tile_src_strided_ool<MODE, SEG>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
+                    accumulate_tile_src_strided_ool<MODE, SEG, POLAR>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
             } else {
                 if constexpr (MODE == kFast)
-                    accumulate_tile<MODE, NPOLY>(rec, sm.coord, sm.run, tid);
+                    accumulate_tile<MODE, NPOLY, POLAR>(rec, sm.coord, sm.run, tid);
                 else
-                    accumulate_tile_ool<MODE, NPOLY>(rec, sm.coord, sm.run, tid);
+                    accumulate_tile_ool<MODE, NPOLY, POLAR>(rec, sm.coord, sm.run, tid);
             }
         }
         __syncwarp();

@@ -22,18 +22,29 @@ def test_defaults(monkeypatch):
 
 
 def test_roofline_counts():
-    # pair by pair: the MUFU pipe binds; 15 of 16 pairs take sin and cos on
-    # it, so 16 / (2 * 15/16) = 8.53 pairs per SM per clock
-    lanes, mufu, issue = bench.per_pair_counts("direct")
-    assert (lanes, mufu, issue) == (7 + 13 / 16, 2 * 15 / 16, 9 - 2 / 16 + 13 / 16)
-    assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct") - 152 * (16 / mufu) * 2070e6) < 1
-    assert 16 / mufu < min(128 / lanes, 128 / issue)
-    lanes, mufu, issue = bench.per_pair_counts("recurrence")
+    # pair by pair: the 16-lane pipe binds; 15 of 16 pairs take sin and cos on
+    # it, so 16 / (2 * 15/16) = 8.53 pairs per SM per clock.  Per pair: the
+    # phase with the weight's phase (3) and the two real FMAs of a polar
+    # weight (2); a hardware-sin/cos pair adds its reduction and 2 pi t (4),
+    # a polynomial pair 12 FP32 operations and 2 sign flips
+    lanes, xu, issue = bench.per_pair_counts("direct")
+    assert (lanes, xu, issue) == (5 + (4 * 15 + 12) / 16, 2 * 15 / 16, 5 + (6 * 15 + 14) / 16)
+    assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct") - 152 * (16 / xu) * 2070e6) < 1
+    assert 16 / xu < min(128 / lanes, 128 / issue)
+    # the recurrence: per target 4 lanes in 2 instructions (the first two
+    # targets take no step), per (thread, sample) 19 lanes, 6 operations on
+    # the 16-lane pipe (4 sin/cos, 2 rintf) and 21 instructions
+    lanes, xu, issue = bench.per_pair_counts("recurrence")
     V = bench.TARGETS_PER_THREAD
-    assert abs(lanes - (4 - 4 / V + 16 / V)) < 1e-12 and abs(mufu - 4 / V) < 1e-12
-    assert abs(issue - (2 + 15 / V)) < 1e-12
+    assert abs(lanes - (4 - 4 / V + 19 / V)) < 1e-12 and abs(xu - 6 / V) < 1e-12
+    assert abs(issue - (2 + 19 / V)) < 1e-12
     # with V = 32 the FP32 lanes bind
     assert abs(bench.peak_pairs_per_s(152, 2070.0, "recurrence") - 152 * (128 / lanes) * 2070e6) < 1
+    # accurate pair by pair: 31 instructions per pair bind
+    lanes, xu, issue = bench.per_pair_counts("direct-accurate")
+    assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct-accurate") - 152 * (128 / issue) * 2070e6) < 1
+    for path in ("source", "recurrence-accurate"):
+        assert all(v > 0 for v in bench.per_pair_counts(path))
 
 
 def test_profiled_traffic_is_guarded():
