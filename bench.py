@@ -146,6 +146,9 @@ def parse():
     ap.add_argument("--mode", choices=["fast", "accurate", "fast-direct", "accurate-direct"], default="fast")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--replicas", action="store_true",
+                    help="with N > 1 GPUs: every rank runs the whole workload as an independent problem (weak "
+                         "scaling) instead of one problem sharded over the ranks (strong scaling, the default)")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the secondary accurate pair-by-pair measurement of the default line")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
@@ -428,11 +431,27 @@ def run_ours(args, world, rank, local):
     fhf = p.op == "fhf"
     if fhf:  # F^H F rho: the forward gather (voxel sources) then the adjoint gather
         path = "direct" if args.mode.endswith("direct") else "fhf"
+    job_pairs = p.pairs  # one problem; with replicas every rank runs its own
+    job_N = p.N
+    # One problem sharded over the ranks (non_cartesian_mri_gather_gb300.sharded):
+    # F^H D by voxel ranges, no exchange; F^H F rho with the image sharded by
+    # voxel ranges and two all-gathers (rho, then F rho) between the passes.
+    shard = world > 1 and not args.replicas
+    n0, n1 = 0, p.N
+    if shard:
+        from non_cartesian_mri_gather_gb300 import sharded
+
+        n0, n1 = sharded.partition(p.N, world, rank)
+        if not fhf:
+            p.x, p.y, p.z = (np.ascontiguousarray(a[n0:n1]) for a in (p.x, p.y, p.z))
+        else:
+            p.rho_r, p.rho_i = (np.ascontiguousarray(a[n0:n1]) for a in (p.rho_r, p.rho_i))
+    n_out = n1 - n0
     names = ("x", "y", "z", "rho_r", "rho_i", "kx", "ky", "kz") if fhf else ("kx", "ky", "kz", "Dr", "Di", "x", "y", "z")
     host = {k: torch.from_numpy(getattr(p, k)) for k in names}
     d = {k: v.to(dev) for k, v in host.items()}
-    rho_r = torch.empty(p.N, dtype=torch.float32, device=dev)
-    rho_i = torch.empty(p.N, dtype=torch.float32, device=dev)
+    rho_r = torch.empty(n_out, dtype=torch.float32, device=dev)
+    rho_i = torch.empty(n_out, dtype=torch.float32, device=dev)
     ws = fhd.Workspace(fhd.OP_FHF if fhf else fhd.OP_FHD, p.N, p.M, local)
     stream = torch.cuda.current_stream(dev)
     shape = fhd.fhd_launch_shape(local, mode)
@@ -445,8 +464,14 @@ def run_ours(args, world, rank, local):
         if fhf:
             if e0 is not None:
                 e0.record(stream)
-            fhd.fhfrho_apply(dd["x"], dd["y"], dd["z"], dd["rho_r"], dd["rho_i"], dd["kx"], dd["ky"], dd["kz"], rr,
-                             ri, mode=mode, workspace=ws)
+            if shard:
+                o_r, o_i = sharded.fhfrho_apply_sharded(dd["x"], dd["y"], dd["z"], dd["rho_r"], dd["rho_i"], dd["kx"],
+                                                        dd["ky"], dd["kz"], mode=mode)
+                rr.copy_(o_r)
+                ri.copy_(o_i)
+            else:
+                fhd.fhfrho_apply(dd["x"], dd["y"], dd["z"], dd["rho_r"], dd["rho_i"], dd["kx"], dd["ky"], dd["kz"],
+                                 rr, ri, mode=mode, workspace=ws)
             if e1 is not None:
                 e1.record(stream)
         elif e0 is None:
@@ -491,8 +516,9 @@ def run_ours(args, world, rank, local):
     ms_local = sum(step_ms) / args.steps
     ms = max_over_ranks(ms_local, world)
     gather_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    pairs = p.pairs
-    value = world * pairs / (ms * 1e-3)
+    pairs = p.pairs if not (shard and fhf) else 2 * n_out * p.M  # this rank's pairs
+    job = job_pairs if shard else world * job_pairs  # pairs all ranks process per step
+    value = job / (ms * 1e-3)
 
     # ---- end to end through the public API with pinned host buffers.  A
     # pipelined client: step k+1's inputs cross host -> device on one stream
@@ -503,8 +529,8 @@ def run_ours(args, world, rank, local):
     e2e = None
     if not args.no_e2e:
         pin = {k: v.pin_memory() for k, v in host.items()}
-        out_r = torch.empty(p.N, dtype=torch.float32).pin_memory()
-        out_i = torch.empty(p.N, dtype=torch.float32).pin_memory()
+        out_r = torch.empty(n_out, dtype=torch.float32).pin_memory()
+        out_i = torch.empty(n_out, dtype=torch.float32).pin_memory()
         bufs = [d, {k: torch.empty_like(v) for k, v in d.items()}]
         outs = [(rho_r, rho_i), (torch.empty_like(rho_r), torch.empty_like(rho_i))]
         h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -577,16 +603,20 @@ def run_ours(args, world, rank, local):
         t3.record(stream)
         torch.cuda.synchronize()
         ms_serial = max_over_ranks(s3.elapsed_time(t3) / k2, world)
-        e2e = {"value": world * pairs / (ms_e2e * 1e-3), "unit": "pairs/s", "h2d_bytes_per_step": input_bytes,
-               "d2h_bytes_per_step": 2 * p.N * 4, "ms_per_step": ms_e2e, "steps": k2,
+        e2e = {"value": job / (ms_e2e * 1e-3), "unit": "pairs/s", "h2d_bytes_per_step": input_bytes,
+               "d2h_bytes_per_step": 2 * n_out * 4, "ms_per_step": ms_e2e, "steps": k2,
                "pipeline": "inputs of step k+1 copied in and the result of step k copied out while step k "
                            "computes (two copy streams, double-buffered device arrays)",
-               "serial": {"value": world * pairs / (ms_serial * 1e-3), "ms_per_step": ms_serial,
+               "serial": {"value": job / (ms_serial * 1e-3), "ms_per_step": ms_serial,
                           "note": "copy in, compute, copy out on one stream, no overlap"}}
 
     if rank != 0:
         return
-    gathers = [(p.M, p.N), (p.N, p.M)] if fhf else [(p.N, p.M)]
+    if fhf:
+        m0, m1 = sharded.partition(p.M, world, rank) if shard else (0, p.M)
+        gathers = [(m1 - m0, p.N), (n_out, p.M)]
+    else:
+        gathers = [(p.N, p.M)]
     launches = sum(gather_launches(fhd, shape, sms, nt, ns) for nt, ns in gathers)
 
     # ---- roofline of the gather kernel (plain-ALU bound)
@@ -674,22 +704,24 @@ def run_ours(args, world, rank, local):
         "ms_per_step_median": float(np.median(step_ms)),
         "ms_per_step_best": min(step_ms),
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if shard else "weak",
         "vs_baseline": None,
         "dtype": "f32",
         "mode": args.mode,
         "data": "synthetic",
         "config": {
             "workload": WORKLOAD_NAMES[args.workload],
-            "N": p.N,
+            "N": job_N,
             "M": p.M,
-            "pairs_per_step": pairs,
+            "pairs_per_step": job,
             "flop_per_pair": FLOP_PER_PAIR,
             "l2": f"inputs exceed L2 ({input_bytes / 2**20:.0f} MiB of inputs vs {L2_BYTES / 2**20:.0f} MiB L2)"
                   if input_bytes > L2_BYTES else
                   f"L2 flushed before every timed step ({2 * L2_BYTES / 2**20:.0f} MiB write outside the step's events)",
             "launch": shape,
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "parallelism": (f"one problem sharded over {world} ranks (voxel ranges"
+                            + (", two all-gathers per step)" if fhf else ", no exchange)")) if shard else
+                           (f"replicas x{world}" if world > 1 else "single GPU"),
         },
         "roofline": roof,
         "secondary": secondary,
