@@ -74,18 +74,25 @@ def per_pair_counts(path: str):
     is two real FMAs."""
     V = TARGETS_PER_THREAD
     if path == "direct":
-        # per pair: k.x + arg(w) (3 FMA-pipe operations), |w| (cos, sin) into
-        # the sums (2 FFMA); 15 of 16 pairs: t = p - rint(p) with the FMA-pipe
-        # rounding (3) and 2 pi t (1), sin and cos on the 16-lane pipe; the
-        # 16th pair: the fast polynomial (half-period reduction 3, u^2 1,
-        # sin 4, cos 4) and 2 sign flips on the integer pipe
-        g = 16.0
-        return 5.0 + (4.0 * (g - 1) + 12.0) / g, 2.0 * (g - 1) / g, 5.0 + (6.0 * (g - 1) + 14.0) / g
+        # per target: k.x + arg(w) (3 FMA-pipe operations) and |w| (cos, sin)
+        # into the sums (2 FFMA); 7 of 8 targets of a group: t = p - rint(p)
+        # with the FMA-pipe rounding (3) and 2 pi t (1), sin and cos on the
+        # 16-lane pipe; the 8th: the fast polynomial (half-period reduction
+        # 3, u^2 1, sin 4, cos 4) and 2 sign flips.  Targets go in packed
+        # f32x2 pairs: the three groups of hardware-sin/cos pairs issue 13
+        # instructions per two targets (3 + 4 + 4 sin/cos + 2), the mixed pair
+        # 25 (3 packed, 6 + 14 per target, 2 packed)
+        g = 8.0
+        return 5.0 + (4.0 * (g - 1) + 12.0) / g, 2.0 * (g - 1) / g, (3 * 13.0 + 25.0) / g
     if path == "direct-accurate":
-        # per pair: the compensated phase (3 FMUL, 3 rintf, 3 FFMA, 3 FADD
+        # per target: the compensated phase (3 FMUL, 3 rintf, 3 FFMA, 3 FADD
         # with arg(w)), the accurate polynomial (half-period reduction 3, u^2
-        # 1, sin 6, cos 5) with 2 sign flips, |w| (cos, sin) into the sums (2)
-        return 26.0, 3.0, 31.0
+        # 1, sin 6, cos 5), |w| (cos, sin) into the sums (2): 26 FP32 lane
+        # operations and 3 rintf; targets in packed pairs: per two targets 12
+        # (the three fractions) + 3 (sums) + 3 (reduction) + 4 (sign flips,
+        # on the weight) + 1 + 6 + 5 (polynomials) + 2 (sums) = 36
+        # instructions
+        return 26.0, 3.0, 18.0
     if path == "source":
         # source-side recurrence (the forward gather: segments of S = 32
         # voxel sources, Cartesian weights), groups of G = 8 targets, packed

@@ -84,6 +84,9 @@ namespace fhd {
 #ifndef FHD_POLAR_WEIGHTS
 #define FHD_POLAR_WEIGHTS 1
 #endif
+#ifndef FHD_DIRECT_PACKED
+#define FHD_DIRECT_PACKED 1
+#endif
 
 constexpr int kThreads = FHD_THREADS;    // consumer threads per CTA
 constexpr int kWarps = kThreads / 32;    // consumer warps
@@ -137,14 +140,15 @@ __host__ __device__ constexpr int segment_len() {
     return MODE == kAccurate ? kSegmentAccurate : kSegment;
 }
 // The pair-by-pair path walks a thread's kV targets in groups (coordinates and
-// per-tile sums of one group in registers at a time): wider in fast mode,
-// where more independent MUFU operations per warp hide their latency, than in
-// accurate mode, whose compensated phase and polynomial need the registers.
+// per-tile sums of one group in registers at a time): 8 in fast mode and 4 in
+// accurate mode, whose compensated phase and polynomial hold more values per
+// target (measured best with the packed path: fast 16 and 4 were 12 % and
+// 12 % slower, accurate 8 and 16 7 % and 11 %).
 #ifndef FHD_DIRECT_GROUP
-#define FHD_DIRECT_GROUP 16
+#define FHD_DIRECT_GROUP 8
 #endif
 #ifndef FHD_DIRECT_GROUP_ACCURATE
-#define FHD_DIRECT_GROUP_ACCURATE 8
+#define FHD_DIRECT_GROUP_ACCURATE 4
 #endif
 template <int MODE>
 __host__ __device__ constexpr int direct_group() {
@@ -575,6 +579,128 @@ __device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
     return d;
 }
 
+// ---------------------------------------------------------------- packed pair-by-pair path
+// Accurate mode, two targets at once: frac(a b) for the packed pair b (see
+// frac_mul), the rounding of each half on the 16-lane pipe.
+__device__ __forceinline__ f2_t frac_mul2(f2_t a, f2_t b) {
+    float h0, h1;
+    f2_unpack(f2_mul(a, b), h0, h1);
+    return f2_fma(a, b, f2_pack(-rintf(h0), -rintf(h1)));
+}
+
+// sincos2pi_poly<true> on a packed pair t: s, c without the sign (-1)^n of
+// the half-period reduction, which is applied to the pair of weights m
+// instead (flipping the weight flips both of its products).
+__device__ __forceinline__ void sincos2pi_poly2_accurate(f2_t t, f2_t& s, f2_t& c, f2_t& m) {
+    const f2_t q = f2_fma(t, f2_pack(2.0f, 2.0f), f2_pack(kRoundMagic, kRoundMagic));
+    const f2_t u = f2_fma(f2_add(q, f2_pack(-kRoundMagic, -kRoundMagic)), f2_pack(-0.5f, -0.5f), t);
+    float q0, q1, m0, m1;
+    f2_unpack(q, q0, q1);
+    f2_unpack(m, m0, m1);
+    m = f2_pack(__uint_as_float(__float_as_uint(m0) ^ (__float_as_uint(q0) << 31)),
+                __uint_as_float(__float_as_uint(m1) ^ (__float_as_uint(q1) << 31)));
+    const f2_t w = f2_mul(u, u);
+    f2_t ps = f2_pack(poly::kAccurateSin[poly::kAccurateSinTerms - 1], poly::kAccurateSin[poly::kAccurateSinTerms - 1]);
+#pragma unroll
+    for (int i = poly::kAccurateSinTerms - 2; i >= 1; --i)
+        ps = f2_fma(ps, w, f2_pack(poly::kAccurateSin[i], poly::kAccurateSin[i]));
+    s = f2_fma(f2_pack(poly::kAccurateSin[0], poly::kAccurateSin[0]), u, f2_mul(f2_mul(u, w), ps));
+    f2_t pc = f2_pack(poly::kAccurateCos[poly::kAccurateCosTerms - 1], poly::kAccurateCos[poly::kAccurateCosTerms - 1]);
+#pragma unroll
+    for (int i = poly::kAccurateCosTerms - 2; i >= 0; --i)
+        pc = f2_fma(pc, w, f2_pack(poly::kAccurateCos[i], poly::kAccurateCos[i]));
+    c = pc;
+}
+
+// The pair-by-pair path on polar records (the adjoint gather) with targets
+// v and v+1 of a group in one packed f32x2 pair: the phase with the weight's
+// phase, its reduction and the two real multiply-accumulates of both targets
+// run as one instruction each (the record holds every coordinate twice, so
+// (A.x, A.x) multiplies (x_v, x_{v+1}) as it stands).  The operations per
+// target are those of accumulate_tile, in about half the issue slots for
+// the FP32 work; the sin/cos stay per target.  In fast mode the last NPOLY
+// (0 or 1) target of a group takes the fast polynomial.
+template <int MODE, int NPOLY>
+__device__ __forceinline__ void accumulate_tile_packed(const float4* __restrict__ rec,
+                                                       const float (*coord)[kThreads], float (*run)[kThreads],
+                                                       int tid) {
+    constexpr int kG = direct_group<MODE>();
+    constexpr int kH = kG / 2;
+    static_assert(kG % 2 == 0 && NPOLY <= 1, "the packed path pairs the targets of a group");
+    const f2_t magic = f2_pack(kRoundMagic, kRoundMagic), nmagic = f2_pack(-kRoundMagic, -kRoundMagic);
+    const f2_t neg1 = f2_pack(-1.0f, -1.0f), two_pi = f2_pack(kTwoPi, kTwoPi);
+#pragma unroll 1
+    for (int g = 0; g < kV; g += kG) {
+        f2_t bx[kH], by[kH], bz[kH], ar[kH], ai[kH];
+#pragma unroll
+        for (int h = 0; h < kH; ++h) {
+            bx[h] = f2_pack(coord[g + 2 * h][tid], coord[g + 2 * h + 1][tid]);
+            by[h] = f2_pack(coord[kV + g + 2 * h][tid], coord[kV + g + 2 * h + 1][tid]);
+            bz[h] = f2_pack(coord[2 * kV + g + 2 * h][tid], coord[2 * kV + g + 2 * h + 1][tid]);
+            ar[h] = 0ull;  // +0.0f in both halves
+            ai[h] = 0ull;
+        }
+#pragma unroll kUnroll
+        for (int s = 0; s < kTile; ++s) {
+            const float4 r0 = rec[2 * s];      // A.x A.x A.y A.y
+            const float4 r1 = rec[2 * s + 1];  // A.z A.z |w| phi
+            const f2_t ax = f2_pack(r0.x, r0.y), ay = f2_pack(r0.z, r0.w), az = f2_pack(r1.x, r1.y);
+            const f2_t phi = f2_pack(r1.w, r1.w);
+#pragma unroll
+            for (int h = 0; h < kH; ++h) {
+                f2_t sn, cs, m = f2_pack(r1.z, r1.z);
+                if constexpr (MODE == kAccurate) {
+                    const f2_t t = f2_add(f2_add(f2_add(frac_mul2(ax, bx[h]), frac_mul2(ay, by[h])),
+                                                 frac_mul2(az, bz[h])), phi);
+                    sincos2pi_poly2_accurate(t, sn, cs, m);
+                } else {
+                    const f2_t p = f2_fma(az, bz[h], f2_fma(ay, by[h], f2_fma(ax, bx[h], phi)));
+                    float s0, c0, s1, c1;
+                    if (NPOLY == 1 && h == kH - 1) {
+                        float p0, p1;
+                        f2_unpack(p, p0, p1);
+                        phasor_mufu(p0, s0, c0);
+                        sincos2pi_poly<false>(p1, s1, c1);
+                    } else {
+                        // t = p - rint(p) (FMA-pipe rounding), 2 pi t, both halves at once
+                        const f2_t th = f2_mul(f2_fma(f2_add(f2_add(p, magic), nmagic), neg1, p), two_pi);
+                        float t0, t1;
+                        f2_unpack(th, t0, t1);
+                        s0 = __sinf(t0);
+                        c0 = __cosf(t0);
+                        s1 = __sinf(t1);
+                        c1 = __cosf(t1);
+                    }
+                    sn = f2_pack(s0, s1);
+                    cs = f2_pack(c0, c1);
+                }
+                ar[h] = f2_fma(m, cs, ar[h]);
+                ai[h] = f2_fma(m, sn, ai[h]);
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < kH; ++h) {
+            float a0, a1, b0, b1;
+            f2_unpack(ar[h], a0, a1);
+            f2_unpack(ai[h], b0, b1);
+            run[g + 2 * h][tid] += a0;
+            run[g + 2 * h + 1][tid] += a1;
+            run[kV + g + 2 * h][tid] += b0;
+            run[kV + g + 2 * h + 1][tid] += b1;
+        }
+    }
+}
+
+// The pair-by-pair path of a gather instantiation: packed on polar records.
+template <int MODE, int NPOLY, bool POLAR>
+__device__ __forceinline__ void direct_tile(const float4* __restrict__ rec, const float (*coord)[kThreads],
+                                            float (*run)[kThreads], int tid) {
+    if constexpr (POLAR && FHD_DIRECT_PACKED)
+        accumulate_tile_packed<MODE, NPOLY>(rec, coord, run, tid);
+    else
+        accumulate_tile<MODE, NPOLY, POLAR>(rec, coord, run, tid);
+}
+
 // Sign of the stored accumulator of target v in the recurrence below.
 __host__ __device__ constexpr bool strided_negated(int v) { return (v & 2) != 0; }
 // Sign of the stored accumulator of target v with the two-chain recurrence:
@@ -936,7 +1062,7 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
 template <int MODE, int NPOLY, bool POLAR>
 __device__ __noinline__ void accumulate_tile_ool(const float4* __restrict__ rec, const float (*coord)[kThreads],
                                                  float (*run)[kThreads], int tid) {
-    accumulate_tile<MODE, NPOLY, POLAR>(rec, coord, run, tid);
+    direct_tile<MODE, NPOLY, POLAR>(rec, coord, run, tid);
 }
 template <int MODE, int SEG, bool POLAR>
 __device__ __noinline__ void accumulate_tile_src_strided_ool(const float4* __restrict__ rec,
@@ -1107,7 +1233,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
                     accumulate_tile_src_strided_ool<MODE, SEG, POLAR>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
             } else {
                 if constexpr (MODE == kFast)
-                    accumulate_tile<MODE, NPOLY, POLAR>(rec, sm.coord, sm.run, tid);
+                    direct_tile<MODE, NPOLY, POLAR>(rec, sm.coord, sm.run, tid);
                 else
                     accumulate_tile_ool<MODE, NPOLY, POLAR>(rec, sm.coord, sm.run, tid);
             }

@@ -22,13 +22,14 @@ def test_defaults(monkeypatch):
 
 
 def test_roofline_counts():
-    # pair by pair: the 16-lane pipe binds; 15 of 16 pairs take sin and cos on
-    # it, so 16 / (2 * 15/16) = 8.53 pairs per SM per clock.  Per pair: the
-    # phase with the weight's phase (3) and the two real FMAs of a polar
-    # weight (2); a hardware-sin/cos pair adds its reduction and 2 pi t (4),
-    # a polynomial pair 12 FP32 operations and 2 sign flips
+    # pair by pair: the 16-lane pipe binds; 7 of 8 targets take sin and cos
+    # on it, so 16 / (2 * 7/8) = 9.14 pairs per SM per clock.  Per target:
+    # the phase with the weight's phase (3) and the two real FMAs of a polar
+    # weight (2); a hardware-sin/cos target adds its reduction and 2 pi t (4),
+    # a polynomial target 12 FP32 operations and 2 sign flips; targets go in
+    # packed pairs (64 instructions per group of 8)
     lanes, xu, issue = bench.per_pair_counts("direct")
-    assert (lanes, xu, issue) == (5 + (4 * 15 + 12) / 16, 2 * 15 / 16, 5 + (6 * 15 + 14) / 16)
+    assert (lanes, xu, issue) == (5 + (4 * 7 + 12) / 8, 2 * 7 / 8, 64 / 8)
     assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct") - 152 * (16 / xu) * 2070e6) < 1
     assert 16 / xu < min(128 / lanes, 128 / issue)
     # the recurrence: per target 4 lanes in 2 instructions (the first two
@@ -40,9 +41,9 @@ def test_roofline_counts():
     assert abs(issue - (2 + 19 / V)) < 1e-12
     # with V = 32 the FP32 lanes bind
     assert abs(bench.peak_pairs_per_s(152, 2070.0, "recurrence") - 152 * (128 / lanes) * 2070e6) < 1
-    # accurate pair by pair: 31 instructions per pair bind
+    # accurate pair by pair: 26 FP32 lane operations per pair bind
     lanes, xu, issue = bench.per_pair_counts("direct-accurate")
-    assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct-accurate") - 152 * (128 / issue) * 2070e6) < 1
+    assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct-accurate") - 152 * (128 / lanes) * 2070e6) < 1
     for path in ("source", "recurrence-accurate"):
         assert all(v > 0 for v in bench.per_pair_counts(path))
 
