@@ -401,6 +401,27 @@ def test_source_recurrence_step_changes_within_tile(mode):
     check(gpu_fhd(p, mode), ref, mode, "F^H D 96-sample spoke sources")
 
 
+# ------------------------------------------------------------ polar weights
+
+@pytest.mark.parametrize("coords", ["uniform", "grid"])
+@pytest.mark.parametrize("mode", ALL_MODES)
+def test_weights_special_values(coords, mode):
+    """The adjoint gather stores each weight as {|w|, arg(w) / 2 pi}: exact
+    zeros, negative and positive reals (arg = 1/2 and 0 cycles), pure
+    imaginary weights (+-1/4), and magnitudes from 1e-30 to 1e30 in one sum,
+    all against the oracle."""
+    p = random_problem(32768 if coords == "grid" else 5000, 1536, kmax=24.0, seed=90, coords=coords)
+    special = np.array([0.0, -1.0, 1.0, 1j, -1j, -0.0, 1e-30, -1e-30j, 2.5 - 0j, -3.0 + 1e-7j], dtype=np.complex128)
+    D = (p.Dr + 1j * p.Di).astype(np.complex128)
+    D[: special.size * 100] = np.tile(special, 100)
+    D[1400:1410] *= 1e30
+    p.Dr, p.Di = D.real.astype(np.float32), D.imag.astype(np.float32)
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    got = gpu_fhd(p, mode)
+    assert np.all(np.isfinite(got))
+    check(got, ref, mode, f"F^H D special weights ({coords})")
+
+
 # ------------------------------------------------------------ edge cases
 
 def test_empty_and_zero_sources():
