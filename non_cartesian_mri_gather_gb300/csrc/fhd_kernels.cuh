@@ -84,9 +84,6 @@ namespace fhd {
 #ifndef FHD_POLAR_WEIGHTS
 #define FHD_POLAR_WEIGHTS 1
 #endif
-#ifndef FHD_DIRECT_PACKED
-#define FHD_DIRECT_PACKED 1
-#endif
 
 constexpr int kThreads = FHD_THREADS;    // consumer threads per CTA
 constexpr int kWarps = kThreads / 32;    // consumer warps
@@ -486,14 +483,15 @@ struct __align__(16) GatherSmem {
     uint64_t empty[kStages];
 };
 
-// Sum of one staged tile over the thread's kV targets, pair by pair: every
-// record is read by all lanes at once (broadcast).  Targets go in groups of
-// direct_group<MODE>() with fresh per-tile accumulators; each group's tile sums are
-// folded into the thread's running sums in shared memory.  In fast mode the
-// last NPOLY slots of a group take the FMA-pipe polynomial, the others the
-// MUFU pipe; accurate mode takes the compensated phase and the accurate
-// polynomial on every pair.
-template <int MODE, int NPOLY, bool POLAR>
+// Sum of one staged tile over the thread's kV targets, pair by pair, on
+// records with Cartesian weights (the forward gather; polar records take
+// accumulate_tile_packed): every record is read by all lanes at once
+// (broadcast).  Targets go in groups of direct_group<MODE>() with fresh
+// per-tile accumulators; each group's tile sums are folded into the thread's
+// running sums in shared memory.  In fast mode the last NPOLY slots of a
+// group take the FMA-pipe polynomial, the others the MUFU pipe; accurate mode
+// takes the compensated phase and the accurate polynomial on every pair.
+template <int MODE, int NPOLY>
 __device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, const float (*coord)[kThreads],
                                                 float (*run)[kThreads], int tid) {
     constexpr int kDirectGroup = direct_group<MODE>();
@@ -520,26 +518,18 @@ __device__ __forceinline__ void accumulate_tile(const float4* __restrict__ rec, 
             for (int v = 0; v < kDirectGroup; ++v) {
                 float sn, cs;
                 if constexpr (MODE == kAccurate) {
-                    if constexpr (POLAR)
-                        phasor_accurate_off(r1.w, r0.x, r0.z, r1.x, bx[v], by[v], bz[v], sn, cs);
-                    else
-                        phasor_accurate(r0.x, r0.z, r1.x, bx[v], by[v], bz[v], sn, cs);
+                    phasor_accurate(r0.x, r0.z, r1.x, bx[v], by[v], bz[v], sn, cs);
                 } else {
-                    const float p = fmaf(r1.x, bz[v], fmaf(r0.z, by[v], POLAR ? fmaf(r0.x, bx[v], r1.w) : r0.x * bx[v]));
+                    const float p = fmaf(r1.x, bz[v], fmaf(r0.z, by[v], r0.x * bx[v]));
                     if (v >= kDirectGroup - NPOLY)
                         sincos2pi_poly<false>(p, sn, cs);
                     else
                         phasor_mufu(p, sn, cs);
                 }
-                if constexpr (POLAR) {  // |w| (cos, sin) of the phase with arg(w) in it
-                    gr[v] = fmaf(r1.z, cs, gr[v]);
-                    gi[v] = fmaf(r1.z, sn, gi[v]);
-                } else {
-                    gr[v] = fmaf(r1.z, cs, gr[v]);
-                    gr[v] = fmaf(-r1.w, sn, gr[v]);
-                    gi[v] = fmaf(r1.z, sn, gi[v]);
-                    gi[v] = fmaf(r1.w, cs, gi[v]);
-                }
+                gr[v] = fmaf(r1.z, cs, gr[v]);
+                gr[v] = fmaf(-r1.w, sn, gr[v]);
+                gi[v] = fmaf(r1.z, sn, gi[v]);
+                gi[v] = fmaf(r1.w, cs, gi[v]);
             }
         }
 #pragma unroll
@@ -691,14 +681,15 @@ __device__ __forceinline__ void accumulate_tile_packed(const float4* __restrict_
     }
 }
 
-// The pair-by-pair path of a gather instantiation: packed on polar records.
+// The pair-by-pair path of a gather instantiation: packed pairs of targets on
+// polar records, one target at a time on Cartesian ones.
 template <int MODE, int NPOLY, bool POLAR>
 __device__ __forceinline__ void direct_tile(const float4* __restrict__ rec, const float (*coord)[kThreads],
                                             float (*run)[kThreads], int tid) {
-    if constexpr (POLAR && FHD_DIRECT_PACKED)
+    if constexpr (POLAR)
         accumulate_tile_packed<MODE, NPOLY>(rec, coord, run, tid);
     else
-        accumulate_tile<MODE, NPOLY, POLAR>(rec, coord, run, tid);
+        accumulate_tile<MODE, NPOLY>(rec, coord, run, tid);
 }
 
 // Sign of the stored accumulator of target v in the recurrence below.
