@@ -84,6 +84,9 @@ namespace fhd {
 #ifndef FHD_POLAR_WEIGHTS
 #define FHD_POLAR_WEIGHTS 1
 #endif
+#ifndef FHD_HORNER_GROUP
+#define FHD_HORNER_GROUP 8
+#endif
 
 constexpr int kThreads = FHD_THREADS;    // consumer threads per CTA
 constexpr int kWarps = kThreads / 32;    // consumer warps
@@ -1044,6 +1047,141 @@ __device__ __forceinline__ void accumulate_tile_src_strided(const float4* __rest
     }
 }
 
+// Source-side sums by Horner's rule, the alternative to the recurrence
+// above for the same tiles.  For target b and segment sources A_s = A_0 + s d
+// (s = 0..S-1): sum_s w_s exp(i 2 pi A_s.b) = e_0 sum_s w_s z^s, with
+// e_0 = exp(i 2 pi A_0.b) and z = exp(i 2 pi d.b).  The polynomial in z is
+// evaluated by Horner's rule from the segment's last source, acc = acc z + w_s
+// (one complex multiply-add per pair, its rounding growing linearly along
+// the segment), then multiplied by e_0 once per (target, segment).  Two
+// targets share every packed f32x2 pair, their real parts in one pair and
+// their imaginary parts in another, so a pair costs two packed FMAs for the
+// real parts and two for the imaginary parts of two targets: 4 FP32 lane
+// operations in 2 instructions (the recurrence takes 6 in 3).  z is
+// evaluated only when a segment's step differs from the previous one's (on
+// an image grid, once per tile), from the phasor of half the step, as there.
+constexpr int kHornerGroup = kV < FHD_HORNER_GROUP ? kV : FHD_HORNER_GROUP;
+static_assert(kV % kHornerGroup == 0 && kHornerGroup % 2 == 0, "Horner's rule pairs the targets of a group");
+
+template <int MODE, int SEG, bool POLAR>
+__device__ __forceinline__ void accumulate_tile_src_horner(const float4* __restrict__ rec,
+                                                           const float4* __restrict__ desc,
+                                                           const float (*coord)[kThreads], float (*run)[kThreads],
+                                                           int tid) {
+    constexpr int kSourceGroup = kHornerGroup;  // targets per group, in kH packed pairs
+    constexpr int kH = kSourceGroup / 2;
+#pragma unroll 1
+    for (int g = 0; g < kV; g += kSourceGroup) {
+        float bx[kSourceGroup], by[kSourceGroup], bz[kSourceGroup];
+#pragma unroll
+        for (int v = 0; v < kSourceGroup; ++v) {
+            bx[v] = coord[g + v][tid];
+            by[v] = coord[kV + g + v][tid];
+            bz[v] = coord[2 * kV + g + v][tid];
+        }
+        f2_t sr[kH], si[kH];  // tile sums: real, imaginary parts of targets 2h, 2h+1
+        f2_t zr[kH], zi[kH], nzi[kH];
+#pragma unroll
+        for (int h = 0; h < kH; ++h) {
+            sr[h] = 0ull;  // +0.0f in both halves
+            si[h] = 0ull;
+        }
+        float4 d_prev = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int j = 0; j < kTile / SEG; ++j) {
+            const float4 d = desc[j];
+            if (j == 0 || d.x != d_prev.x || d.y != d_prev.y || d.z != d_prev.z) {  // uniform over the CTA
+                const float hx = 0.5f * d.x, hy = 0.5f * d.y, hz = 0.5f * d.z;
+                float cu[kSourceGroup], su[kSourceGroup];
+#pragma unroll
+                for (int v = 0; v < kSourceGroup; ++v) {
+                    float sh, ch;
+                    if constexpr (MODE == kAccurate) {
+                        phasor_step_accurate(hx, hy, hz, bx[v], by[v], bz[v], sh, ch);
+                        cu[v] = fabsf(sh) < fabsf(ch) ? fmaf(-2.0f * sh, sh, 1.0f) : fmaf(2.0f * ch, ch, -1.0f);
+                    } else {
+                        phasor_mufu(fmaf(hz, bz[v], fmaf(hy, by[v], hx * bx[v])), sh, ch);
+                        cu[v] = fmaf(-2.0f * sh, sh, 1.0f);
+                    }
+                    su[v] = (sh + sh) * ch;
+                }
+#pragma unroll
+                for (int h = 0; h < kH; ++h) {
+                    zr[h] = f2_pack(cu[2 * h], cu[2 * h + 1]);
+                    zi[h] = f2_pack(su[2 * h], su[2 * h + 1]);
+                    nzi[h] = f2_pack(-su[2 * h], -su[2 * h + 1]);
+                }
+                d_prev = d;
+            }
+            f2_t ar[kH], ai[kH];
+            {  // Horner's rule starts from the segment's last weight
+                const float4 r = rec[2 * (j * SEG + SEG - 1) + 1];
+                const float2 w = record_weight<MODE, POLAR>(r.z, r.w);
+#pragma unroll
+                for (int h = 0; h < kH; ++h) {
+                    ar[h] = f2_pack(w.x, w.x);
+                    ai[h] = f2_pack(w.y, w.y);
+                }
+            }
+#pragma unroll
+            for (int s = SEG - 2; s >= 0; --s) {
+                const float4 r = rec[2 * (j * SEG + s) + 1];  // the weight in .z, .w
+                const float2 w = record_weight<MODE, POLAR>(r.z, r.w);
+                const f2_t wr = f2_pack(w.x, w.x), wi = f2_pack(w.y, w.y);
+#pragma unroll
+                for (int h = 0; h < kH; ++h) {
+                    const f2_t nr = f2_fma(zr[h], ar[h], f2_fma(nzi[h], ai[h], wr));  // (acc z + w).re
+                    const f2_t ni = f2_fma(zr[h], ai[h], f2_fma(zi[h], ar[h], wi));   // (acc z + w).im
+                    ar[h] = nr;
+                    ai[h] = ni;
+                }
+            }
+            // times e_0 = exp(i 2 pi A_0.b), into the tile sums
+            const float4 b0 = rec[2 * j * SEG];      // A_0.x A_0.x A_0.y A_0.y
+            const float4 b1 = rec[2 * j * SEG + 1];  // A_0.z A_0.z w
+            float c0[kSourceGroup], s0[kSourceGroup];
+#pragma unroll
+            for (int v = 0; v < kSourceGroup; ++v) {
+                if constexpr (MODE == kAccurate)
+                    phasor_accurate(b0.x, b0.z, b1.x, bx[v], by[v], bz[v], s0[v], c0[v]);
+                else
+                    phasor_mufu(fmaf(b1.x, bz[v], fmaf(b0.z, by[v], b0.x * bx[v])), s0[v], c0[v]);
+            }
+#pragma unroll
+            for (int h = 0; h < kH; ++h) {
+                const f2_t c = f2_pack(c0[2 * h], c0[2 * h + 1]);
+                const f2_t sn = f2_pack(s0[2 * h], s0[2 * h + 1]), nsn = f2_pack(-s0[2 * h], -s0[2 * h + 1]);
+                sr[h] = f2_fma(c, ar[h], f2_fma(nsn, ai[h], sr[h]));
+                si[h] = f2_fma(c, ai[h], f2_fma(sn, ar[h], si[h]));
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < kH; ++h) {
+            float r0v, r1v, i0v, i1v;
+            f2_unpack(sr[h], r0v, r1v);
+            f2_unpack(si[h], i0v, i1v);
+            run[g + 2 * h][tid] += r0v;
+            run[g + 2 * h + 1][tid] += r1v;
+            run[kV + g + 2 * h][tid] += i0v;
+            run[kV + g + 2 * h + 1][tid] += i1v;
+        }
+    }
+}
+
+// The source-side path of a gather instantiation: Horner's rule in the
+// forward gathers (Cartesian records), whose tiles take this path; the
+// recurrence in the adjoint gathers, where it is rare and where the
+// recurrence measured faster for the kernel as a whole (the fast adjoint
+// kernel inlines this path next to its hot target-side loop).
+template <int MODE, int SEG, bool POLAR>
+__device__ __forceinline__ void source_tile(const float4* __restrict__ rec, const float4* __restrict__ desc,
+                                            const float (*coord)[kThreads], float (*run)[kThreads], int tid) {
+    if constexpr (!POLAR)
+        accumulate_tile_src_horner<MODE, SEG, POLAR>(rec, desc, coord, run, tid);
+    else
+        accumulate_tile_src_strided<MODE, SEG, POLAR>(rec, desc, coord, run, tid);
+}
+
 // Out-of-line entry points of the pair-by-pair and source-side paths.  The
 // gather kernel is one function holding all three paths, and the register
 // allocation and scheduling of its hot loop depend on what else is inlined
@@ -1060,7 +1198,7 @@ __device__ __noinline__ void accumulate_tile_src_strided_ool(const float4* __res
                                                              const float4* __restrict__ desc,
                                                              const float (*coord)[kThreads],
                                                              float (*run)[kThreads], int tid) {
-    accumulate_tile_src_strided<MODE, SEG, POLAR>(rec, desc, coord, run, tid);
+    source_tile<MODE, SEG, POLAR>(rec, desc, coord, run, tid);
 }
 
 // MODE: kAccurate or kFast.  NPOLY (fast mode only): how many of the kV
@@ -1219,7 +1357,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
                 src_strided = src_strided && sm.desc[st][q].w != 0.f;
             if (src_strided) {
                 if constexpr (MODE == kFast)
-                    accumulate_tile_src_strided<MODE, SEG, POLAR>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
+                    source_tile<MODE, SEG, POLAR>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
                 else
                     accumulate_tile_src_strided_ool<MODE, SEG, POLAR>(rec, &sm.desc[st][0], sm.coord, sm.run, tid);
             } else {
