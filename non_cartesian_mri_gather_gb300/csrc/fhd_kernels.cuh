@@ -34,11 +34,13 @@
 //                       take a recurrence instead of a sin/cos per pair
 //                       (accumulate_tile_strided); otherwise tiles of equally
 //                       spaced source segments (described by
-//                       describe_segments) a source-side recurrence
-//                       (accumulate_tile_src_strided); otherwise pair by pair
-//                       (accumulate_tile).  Instantiated per mode and source
-//                       segment length: the fast adjoint gather, the fast
-//                       forward gather and the accurate gather.
+//                       describe_segments) a source-side evaluation
+//                       (source_tile: Horner's rule in the forward gather, a
+//                       recurrence in the adjoint gather); otherwise pair by
+//                       pair (direct_tile).  Instantiated per mode, source
+//                       segment length and weight form: the adjoint gathers
+//                       (polar weights) and the forward gathers (Cartesian
+//                       weights) of each mode.
 //   3. fixup_kernel   - target blocks whose source range was split between
 //                       CTAs are summed from per-CTA partials in a fixed
 //                       order (no atomics, bit-reproducible).
