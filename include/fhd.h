@@ -73,11 +73,13 @@
  *            exp(i 2 pi k.(x0 + v d)) = exp(i 2 pi k.x0) exp(i 2 pi k.d)^v,
  *            an exact identity evaluated in fp32 (same tolerances).  Other
  *            targets are evaluated pair by pair.  Likewise, where runs of
- *            16 (fast mode) or 32 (accurate mode) consecutive sources are
- *            exactly equally spaced (the voxels of a grid row as sources of
- *            F rho), each target evaluates one phasor per run (two when the
- *            run's step changes) and steps the rest by the same recurrence.  FHD_MODE_DIRECT forces the
- *            pair-by-pair evaluation everywhere.
+ *            consecutive sources are exactly equally spaced (32 voxels of a
+ *            grid row as sources of F rho; 16 or 32 samples along a straight
+ *            line as sources of F^H D), each target evaluates one phasor per
+ *            run (two when the run's step changes) and reaches the rest by
+ *            powers of the step phasor: Horner's rule in F rho, the same
+ *            recurrence in F^H D.  FHD_MODE_DIRECT forces the pair-by-pair
+ *            evaluation everywhere.
  * Small      problems too small to occupy the persistent kernel (a few blocks
  *            of 8192 targets times a few tiles of 256 sources) are evaluated
  *            pair by pair with one target per thread and the sources split
