@@ -75,15 +75,15 @@ def per_pair_counts(path: str):
     V = TARGETS_PER_THREAD
     if path == "direct":
         # per target: k.x + arg(w) (3 FMA-pipe operations) and |w| (cos, sin)
-        # into the sums (2 FFMA); 7 of 8 targets of a group: t = p - rint(p)
+        # into the sums (2 FFMA); 6 of 8 targets of a group: t = p - rint(p)
         # with the FMA-pipe rounding (3) and 2 pi t (1), sin and cos on the
-        # 16-lane pipe; the 8th: the fast polynomial (half-period reduction
-        # 3, u^2 1, sin 4, cos 4) and 2 sign flips.  Targets go in packed
-        # f32x2 pairs: the three groups of hardware-sin/cos pairs issue 13
-        # instructions per two targets (3 + 4 + 4 sin/cos + 2), the mixed pair
-        # 25 (3 packed, 6 + 14 per target, 2 packed)
+        # 16-lane pipe; the other 2 (one packed pair): the fast polynomial
+        # (half-period reduction 3, u^2 1, sin 4, cos 4) with the sign flips
+        # on the weight.  Targets go in packed f32x2 pairs: 13 instructions per
+        # hardware-sin/cos pair of targets (3 + 4 + 4 sin/cos + 2), 22 for the
+        # polynomial pair (3 + 12 + 5 + 2)
         g = 8.0
-        return 5.0 + (4.0 * (g - 1) + 12.0) / g, 2.0 * (g - 1) / g, (3 * 13.0 + 25.0) / g
+        return 5.0 + (4.0 * 6 + 12.0 * 2) / g, 2.0 * 6 / g, (3 * 13.0 + 22.0) / g
     if path == "direct-accurate":
         # per target: the compensated phase (3 FMUL, 3 rintf, 3 FFMA, 3 FADD
         # with arg(w)), the accurate polynomial (half-period reduction 3, u^2

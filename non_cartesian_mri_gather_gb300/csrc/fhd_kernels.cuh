@@ -78,7 +78,7 @@ namespace fhd {
 #define FHD_MIN_CTAS_PER_SM 1
 #endif
 #ifndef FHD_FAST_POLY_SLOTS
-#define FHD_FAST_POLY_SLOTS 1
+#define FHD_FAST_POLY_SLOTS 2
 #endif
 #ifndef FHD_UNROLL
 #define FHD_UNROLL 4
@@ -160,7 +160,11 @@ __host__ __device__ constexpr int direct_group() {
 }
 static_assert(kV % direct_group<kFast>() == 0 && kV % direct_group<kAccurate>() == 0,
               "kV must be a multiple of the direct-path groups");
-constexpr int kFastPolySlots = FHD_FAST_POLY_SLOTS;  // of a fast group: share of sin/cos on the FMA pipe
+// Of a fast pair-by-pair group of 8 targets, how many take the FMA-pipe
+// polynomial instead of the hardware sin/cos: 2 (one packed pair) balances
+// the FP32 pipe (11 lane operations per pair) against the 16-lane sin/cos
+// pipe (1.5 per pair); measured 9 % faster than 1.
+constexpr int kFastPolySlots = FHD_FAST_POLY_SLOTS;
 static_assert(kFastPolySlots >= 0 && kFastPolySlots <= direct_group<kFast>(), "bad polynomial split");
 // The source-side recurrence walks a thread's targets in groups of kSourceGroup.
 #ifndef FHD_SOURCE_GROUP
@@ -583,10 +587,11 @@ __device__ __forceinline__ f2_t frac_mul2(f2_t a, f2_t b) {
     return f2_fma(a, b, f2_pack(-rintf(h0), -rintf(h1)));
 }
 
-// sincos2pi_poly<true> on a packed pair t: s, c without the sign (-1)^n of
+// sincos2pi_poly<ACC> on a packed pair t: s, c without the sign (-1)^n of
 // the half-period reduction, which is applied to the pair of weights m
 // instead (flipping the weight flips both of its products).
-__device__ __forceinline__ void sincos2pi_poly2_accurate(f2_t t, f2_t& s, f2_t& c, f2_t& m) {
+template <bool ACC>
+__device__ __forceinline__ void sincos2pi_poly2(f2_t t, f2_t& s, f2_t& c, f2_t& m) {
     const f2_t q = f2_fma(t, f2_pack(2.0f, 2.0f), f2_pack(kRoundMagic, kRoundMagic));
     const f2_t u = f2_fma(f2_add(q, f2_pack(-kRoundMagic, -kRoundMagic)), f2_pack(-0.5f, -0.5f), t);
     float q0, q1, m0, m1;
@@ -595,16 +600,31 @@ __device__ __forceinline__ void sincos2pi_poly2_accurate(f2_t t, f2_t& s, f2_t& 
     m = f2_pack(__uint_as_float(__float_as_uint(m0) ^ (__float_as_uint(q0) << 31)),
                 __uint_as_float(__float_as_uint(m1) ^ (__float_as_uint(q1) << 31)));
     const f2_t w = f2_mul(u, u);
-    f2_t ps = f2_pack(poly::kAccurateSin[poly::kAccurateSinTerms - 1], poly::kAccurateSin[poly::kAccurateSinTerms - 1]);
+    if constexpr (ACC) {
+        f2_t ps = f2_pack(poly::kAccurateSin[poly::kAccurateSinTerms - 1],
+                          poly::kAccurateSin[poly::kAccurateSinTerms - 1]);
 #pragma unroll
-    for (int i = poly::kAccurateSinTerms - 2; i >= 1; --i)
-        ps = f2_fma(ps, w, f2_pack(poly::kAccurateSin[i], poly::kAccurateSin[i]));
-    s = f2_fma(f2_pack(poly::kAccurateSin[0], poly::kAccurateSin[0]), u, f2_mul(f2_mul(u, w), ps));
-    f2_t pc = f2_pack(poly::kAccurateCos[poly::kAccurateCosTerms - 1], poly::kAccurateCos[poly::kAccurateCosTerms - 1]);
+        for (int i = poly::kAccurateSinTerms - 2; i >= 1; --i)
+            ps = f2_fma(ps, w, f2_pack(poly::kAccurateSin[i], poly::kAccurateSin[i]));
+        s = f2_fma(f2_pack(poly::kAccurateSin[0], poly::kAccurateSin[0]), u, f2_mul(f2_mul(u, w), ps));
+        f2_t pc = f2_pack(poly::kAccurateCos[poly::kAccurateCosTerms - 1],
+                          poly::kAccurateCos[poly::kAccurateCosTerms - 1]);
 #pragma unroll
-    for (int i = poly::kAccurateCosTerms - 2; i >= 0; --i)
-        pc = f2_fma(pc, w, f2_pack(poly::kAccurateCos[i], poly::kAccurateCos[i]));
-    c = pc;
+        for (int i = poly::kAccurateCosTerms - 2; i >= 0; --i)
+            pc = f2_fma(pc, w, f2_pack(poly::kAccurateCos[i], poly::kAccurateCos[i]));
+        c = pc;
+    } else {
+        f2_t ps = f2_pack(poly::kFastSin[poly::kFastSinTerms - 1], poly::kFastSin[poly::kFastSinTerms - 1]);
+#pragma unroll
+        for (int i = poly::kFastSinTerms - 2; i >= 0; --i)
+            ps = f2_fma(ps, w, f2_pack(poly::kFastSin[i], poly::kFastSin[i]));
+        s = f2_mul(ps, u);
+        f2_t pc = f2_pack(poly::kFastCos[poly::kFastCosTerms - 1], poly::kFastCos[poly::kFastCosTerms - 1]);
+#pragma unroll
+        for (int i = poly::kFastCosTerms - 2; i >= 0; --i)
+            pc = f2_fma(pc, w, f2_pack(poly::kFastCos[i], poly::kFastCos[i]));
+        c = pc;
+    }
 }
 
 // The pair-by-pair path on polar records (the adjoint gather) with targets
@@ -614,14 +634,15 @@ __device__ __forceinline__ void sincos2pi_poly2_accurate(f2_t t, f2_t& s, f2_t& 
 // (A.x, A.x) multiplies (x_v, x_{v+1}) as it stands).  The operations per
 // target are those of accumulate_tile, in about half the issue slots for
 // the FP32 work; the sin/cos stay per target.  In fast mode the last NPOLY
-// (0 or 1) target of a group takes the fast polynomial.
+// (0, 1 or 2) targets of a group take the fast polynomial (with 2, both
+// halves of the last pair, in packed arithmetic).
 template <int MODE, int NPOLY>
 __device__ __forceinline__ void accumulate_tile_packed(const float4* __restrict__ rec,
                                                        const float (*coord)[kThreads], float (*run)[kThreads],
                                                        int tid) {
     constexpr int kG = direct_group<MODE>();
     constexpr int kH = kG / 2;
-    static_assert(kG % 2 == 0 && NPOLY <= 1, "the packed path pairs the targets of a group");
+    static_assert(kG % 2 == 0 && NPOLY <= 2, "the packed path pairs the targets of a group");
     const f2_t magic = f2_pack(kRoundMagic, kRoundMagic), nmagic = f2_pack(-kRoundMagic, -kRoundMagic);
     const f2_t neg1 = f2_pack(-1.0f, -1.0f), two_pi = f2_pack(kTwoPi, kTwoPi);
 #pragma unroll 1
@@ -647,7 +668,10 @@ __device__ __forceinline__ void accumulate_tile_packed(const float4* __restrict_
                 if constexpr (MODE == kAccurate) {
                     const f2_t t = f2_add(f2_add(f2_add(frac_mul2(ax, bx[h]), frac_mul2(ay, by[h])),
                                                  frac_mul2(az, bz[h])), phi);
-                    sincos2pi_poly2_accurate(t, sn, cs, m);
+                    sincos2pi_poly2<true>(t, sn, cs, m);
+                } else if (NPOLY == 2 && h == kH - 1) {  // both targets of the last pair on the polynomial
+                    const f2_t p = f2_fma(az, bz[h], f2_fma(ay, by[h], f2_fma(ax, bx[h], phi)));
+                    sincos2pi_poly2<false>(p, sn, cs, m);
                 } else {
                     const f2_t p = f2_fma(az, bz[h], f2_fma(ay, by[h], f2_fma(ax, bx[h], phi)));
                     float s0, c0, s1, c1;

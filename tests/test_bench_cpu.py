@@ -22,14 +22,14 @@ def test_defaults(monkeypatch):
 
 
 def test_roofline_counts():
-    # pair by pair: the 16-lane pipe binds; 7 of 8 targets take sin and cos
-    # on it, so 16 / (2 * 7/8) = 9.14 pairs per SM per clock.  Per target:
+    # pair by pair: the 16-lane pipe binds; 6 of 8 targets take sin and cos
+    # on it, so 16 / (2 * 6/8) = 10.7 pairs per SM per clock.  Per target:
     # the phase with the weight's phase (3) and the two real FMAs of a polar
     # weight (2); a hardware-sin/cos target adds its reduction and 2 pi t (4),
-    # a polynomial target 12 FP32 operations and 2 sign flips; targets go in
-    # packed pairs (64 instructions per group of 8)
+    # a polynomial target 12 FP32 operations; targets go in packed pairs (61
+    # instructions per group of 8)
     lanes, xu, issue = bench.per_pair_counts("direct")
-    assert (lanes, xu, issue) == (5 + (4 * 7 + 12) / 8, 2 * 7 / 8, 64 / 8)
+    assert (lanes, xu, issue) == (5 + (4 * 6 + 12 * 2) / 8, 2 * 6 / 8, 61 / 8)
     assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct") - 152 * (16 / xu) * 2070e6) < 1
     assert 16 / xu < min(128 / lanes, 128 / issue)
     # the recurrence: per target 4 lanes in 2 instructions (the first two
