@@ -108,17 +108,18 @@ def per_pair_counts(path: str):
         S, G = 32.0, 8.0
         return 4.0 + 11.0 / S, 2.0 / S, 2.0 + 13.0 / S + 3.0 / G
     if path == "recurrence-accurate":
-        # the two-chain recurrence of accurate mode with the step phasor
-        # shared by the warp: per (thread, sample) the compensated phase of
-        # the anchor (9 FMA-pipe operations, 3 rintf), the accurate
-        # polynomial (15, 2 sign flips), g_0 = |w| (cos, sin) (2), g_1 (4),
-        # 2 cos (1), the coefficient 2 cos 2 theta chosen from sin or cos (5),
-        # the first two steps (4 lanes), 2 shuffles, and 1/32 of the step
-        # phasor (its compensated phase and sincospif, about 47 operations);
-        # per target the packed add and step (4 lanes, 2 instructions)
-        lanes = 4.0 - 4.0 / V + (9 + 15 + 2 + 4 + 1 + 5 + 4 + 47.0 / 32) / V
+        # the two-chain recurrence of accurate mode with the step phasor and
+        # the chain coefficient shared by the warp: per (thread, sample) the
+        # compensated phase of the anchor with the weight's phase (9 FMA-pipe
+        # operations, 3 rintf), the accurate polynomial (15, 2 sign flips),
+        # g_0 = |w| (cos, sin) (2), g_1 (4), 2 cos(theta_d) (1), 3 shuffles,
+        # and 1/32 of the owner lane's work (the step's compensated phase and
+        # sincospif, the coefficient: about 52 operations); per target the
+        # packed add and step (4 lanes, 2 instructions; no step for the first
+        # two targets)
+        lanes = 4.0 - 4.0 / V + (9 + 15 + 2 + 4 + 1 + 52.0 / 32) / V
         xu = (3.0 + 3.0 / 32) / V
-        issue = 2.0 + (-2 + 12 + 17 + 2 + 4 + 1 + 5 + 2 + 2 + 50.0 / 32) / V
+        issue = 2.0 + (-2 + 12 + 17 + 2 + 4 + 1 + 3 + 55.0 / 32) / V
         return lanes, xu, issue
     # recurrence (fast mode), V targets per thread, as two chains (even and
     # odd targets).  Per (thread, sample): the two phases as 3 packed

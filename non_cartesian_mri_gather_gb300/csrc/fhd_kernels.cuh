@@ -830,31 +830,37 @@ __device__ __forceinline__ void accumulate_tile_strided(const float4* __restrict
     }
 }
 
-// Accurate mode, every lane of the warp with the same target spacing d: the
-// step phasor u_s = exp(i 2 pi a_s.d) is the same for all lanes, so lane l
-// evaluates it for sources 32k + l only and the others read it by shuffle.
-// Phases and sin/cos are those of accumulate_tile_strided (the same
-// operations in the same order), so the sums are bit-identical to it, with
-// 1/32 of the sin/cos evaluations for u.
-template <bool POLAR>
+// Accurate mode, every lane of the warp with the same target spacing d (every
+// warp of an image grid): the step phasor u_s = exp(i 2 pi a_s.d) and the
+// chain coefficient 2 cos(2 theta_d) are the same for all lanes, so lane l
+// evaluates them for sources 32k + l only and the others read them by
+// shuffle.  Phases, sin/cos and coefficients are those of
+// accumulate_tile_strided (the same operations in the same order), so the
+// sums are bit-identical to it, with 1/32 of the sincospif evaluations of
+// the step and of the coefficient's selection.  (Fast mode keeps the
+// per-lane form: its step phasor is cheap, and the shuffles on the chain's
+// critical path measured 1-7 % slower for every unroll factor tried.)
+template <int MODE, bool POLAR>
 __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* __restrict__ rec, float x0,
                                                                  float y0, float z0, float dx, float dy, float dz,
                                                                  int lane, f2_t (&acc)[kV]) {
     static_assert(kTile % 32 == 0, "tiles hold whole warps of sources");
+    static_assert(MODE == kAccurate, "the fast kernel evaluates the step phasor per lane");
 #pragma unroll
     for (int v = 0; v < kV; ++v) acc[v] = 0ull;  // +0.0f in both halves
 #pragma unroll 1
     for (int s32 = 0; s32 < kTile; s32 += 32) {
-        float su_l, cu_l;
+        float su_l, cu_l, cc_l;
         {
             const float4 r0 = rec[2 * (s32 + lane)];
             const float4 r1 = rec[2 * (s32 + lane) + 1];
             phasor_step_accurate(r0.y, r0.w, r1.y, dx, dy, dz, su_l, cu_l);
+            cc_l = two_cos_double(su_l, cu_l);
         }
 #pragma unroll kUnrollSharedU
         for (int q = 0; q < 32; ++q) {
             const float4 r0 = rec[2 * (s32 + q)];      // A.x A.x A.y A.y
-            const float4 r1 = rec[2 * (s32 + q) + 1];  // A.z A.z w.re w.im
+            const float4 r1 = rec[2 * (s32 + q) + 1];  // A.z A.z w
             float s0, c0;
             if constexpr (POLAR)
                 phasor_accurate_off(r1.w, r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
@@ -862,6 +868,7 @@ __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* _
                 phasor_accurate(r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
             const float sw = __shfl_sync(0xffffffffu, su_l, q);
             const float cw = __shfl_sync(0xffffffffu, cu_l, q);
+            const float cc = __shfl_sync(0xffffffffu, cc_l, q);  // 2 cos(2 theta_d)
             // g_0 = w_s * exp(i 2 pi a.b_0)
             const float fr = POLAR ? r1.z * c0 : fmaf(r1.z, c0, -r1.w * s0);
             const float fi = POLAR ? r1.z * s0 : fmaf(r1.z, s0, r1.w * c0);
@@ -872,7 +879,6 @@ __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* _
             const f2_t e0 = f2_pack(fr, fi), e1 = f2_pack(gr, gi);
             const f2_t e2n = f2_fma(f2_pack(-c2, -c2), e1, e0);  // -e_2
             const f2_t e3n = f2_fma(kpos, e2n, e1);              // -e_3
-            const float cc = two_cos_double(sw, cw);              // 2 cos(2 theta_d)
             const f2_t kposC = f2_pack(cc, cc), knegC = f2_pack(-cc, -cc);
             f2_t amA = e0, aA = e2n, amB = e1, aB = e3n;           // chains over even and odd targets
             acc[0] = f2_add(acc[0], e0);
@@ -901,10 +907,14 @@ __device__ __forceinline__ void strided_tile(const float4* __restrict__ rec, flo
                                              float dx, float dy, float dz, int lane, bool shared_u,
                                              float (*run)[kThreads], int tid) {
     f2_t acc[kV];
-    if (MODE == kAccurate && shared_u)
-        accumulate_tile_strided_shared_u<POLAR>(rec, x0, y0, z0, dx, dy, dz, lane, acc);
-    else
+    if constexpr (MODE == kAccurate) {
+        if (shared_u)
+            accumulate_tile_strided_shared_u<MODE, POLAR>(rec, x0, y0, z0, dx, dy, dz, lane, acc);
+        else
+            accumulate_tile_strided<MODE, TWO, POLAR>(rec, x0, y0, z0, dx, dy, dz, acc);
+    } else {
         accumulate_tile_strided<MODE, TWO, POLAR>(rec, x0, y0, z0, dx, dy, dz, acc);
+    }
 #pragma unroll
     for (int v = 0; v < kV; ++v) {
         float re, im;
@@ -1360,7 +1370,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
             } else {
                 f2_t acc[kV];
                 if (shared_u)
-                    accumulate_tile_strided_shared_u<POLAR>(rec, x0, y0, z0, sx, sy, sz, lane, acc);
+                    accumulate_tile_strided_shared_u<MODE, POLAR>(rec, x0, y0, z0, sx, sy, sz, lane, acc);
                 else
                     accumulate_tile_strided<MODE, kTwoChains, POLAR>(rec, x0, y0, z0, sx, sy, sz, acc);
 #pragma unroll
