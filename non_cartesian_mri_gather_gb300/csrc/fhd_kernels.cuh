@@ -100,7 +100,7 @@ constexpr int kRecordBytes = 32;         // one packed source
 constexpr int kTileBytes = kTile * kRecordBytes;
 // Source segments: kSegment consecutive packed sources (fast mode; accurate
 // mode's length is set below) whose coordinates are exactly equally spaced
-// take the source-side recurrence; one 16-byte descriptor {step.x, step.y,
+// take the source-side path; one 16-byte descriptor {step.x, step.y,
 // step.z, flag} per segment, at most kDescBytes per tile.
 constexpr int kSegment = 16;
 constexpr int kSegmentsPerTile = kTile / kSegment;
@@ -116,8 +116,8 @@ constexpr int kUnrollSharedU = 12;       // the same in the accurate warp-shared
 constexpr int kUnrollTwoChains = 6;
 constexpr int kUnrollOneChain = 3;
 // The adjoint gathers store each weight in polar form, {|w|, arg(w) / 2 pi}
-// (see pack_sources); the forward gathers, whose voxel weights feed the
-// source-side recurrence's real-weighted sums, keep {w.re, w.im}.
+// (see pack_sources); the forward gathers, whose voxel weights Horner's rule
+// adds as complex numbers, keep {w.re, w.im}.
 constexpr bool kPolarAdjoint = FHD_POLAR_WEIGHTS != 0;
 static_assert(kThreads % 32 == 0 && kTile % 2 == 0 && kStages >= 2, "bad launch shape");
 
@@ -127,11 +127,12 @@ constexpr uint32_t kStatusProducerTimeout = 2u;
 constexpr uint32_t kStatusDrainTimeout = 4u;
 
 enum Mode : int { kAccurate = 0, kFast = 1 };
-// Source segments are kSegment sources long in fast mode and
-// kSegmentAccurate in accurate mode, where the longer segment halves the
-// per-(target, segment) sin/cos cost of the source-side recurrence (its
-// three-term error bound, eps * s^2 / 2, stays below 3e-5 over 32 sources);
-// the descriptor array is sized for kSegment.
+// Source segments are kSegment sources long in the fast adjoint gather and
+// kSegmentAccurate elsewhere, where the longer segment halves the
+// per-(target, segment) sin/cos cost of the source side (the recurrence's
+// three-term error bound, eps * s^2 / 2, stays below 3e-5 over 32 sources;
+// Horner's rule grows only linearly); the descriptor array is sized for
+// kSegment.
 constexpr int kSegmentAccurate = 32;
 static_assert(kTile % kSegmentAccurate == 0, "tiles hold whole segments");
 // Segment length of the adjoint gather in each mode; the forward gather
@@ -144,7 +145,7 @@ __host__ __device__ constexpr int segment_len() {
 // The pair-by-pair path walks a thread's kV targets in groups (coordinates and
 // per-tile sums of one group in registers at a time): 8 in fast mode and 4 in
 // accurate mode, whose compensated phase and polynomial hold more values per
-// target (measured best with the packed path: fast 16 and 4 were 12 % and
+// target (measured best with the packed path: fast 16 and 4 were 11 % and
 // 12 % slower, accurate 8 and 16 7 % and 11 %).
 #ifndef FHD_DIRECT_GROUP
 #define FHD_DIRECT_GROUP 8
@@ -166,7 +167,9 @@ static_assert(kV % direct_group<kFast>() == 0 && kV % direct_group<kAccurate>() 
 // pipe (1.5 per pair); measured 9 % faster than 1.
 constexpr int kFastPolySlots = FHD_FAST_POLY_SLOTS;
 static_assert(kFastPolySlots >= 0 && kFastPolySlots <= direct_group<kFast>(), "bad polynomial split");
-// The source-side recurrence walks a thread's targets in groups of kSourceGroup.
+// The source-side recurrence (adjoint gathers) walks a thread's targets in
+// groups of kSourceGroup; Horner's rule (forward gathers) in groups of
+// kHornerGroup (below).
 #ifndef FHD_SOURCE_GROUP
 #define FHD_SOURCE_GROUP 8
 #endif
