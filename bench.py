@@ -108,31 +108,51 @@ def per_pair_counts(path: str):
         S, G = 32.0, 8.0
         return 4.0 + 11.0 / S, 2.0 / S, 2.0 + 13.0 / S + 3.0 / G
     if path == "recurrence-accurate":
-        # the two-chain recurrence of accurate mode with the step phasor and
-        # the chain coefficient shared by the warp: per (thread, sample) the
-        # compensated phase of the anchor with the weight's phase (9 FMA-pipe
-        # operations, 3 rintf), the accurate polynomial (15, 2 sign flips),
-        # g_0 = |w| (cos, sin) (2), g_1 (4), 2 cos(theta_d) (1), 3 shuffles,
-        # and 1/32 of the owner lane's work (the step's compensated phase and
-        # sincospif, the coefficient: about 52 operations); per target the
-        # packed add and step (4 lanes, 2 instructions; no step for the first
-        # two targets)
+        # the two-chain recurrence of accurate mode on an image grid: the step
+        # phasor u and the chain coefficients come from the tile's step
+        # records (evaluated once per sample by the pack kernel); per (thread,
+        # sample) the compensated phase of the anchor with the weight's phase
+        # (9 FMA-pipe operations, 3 rintf), the accurate polynomial (15, 2
+        # sign flips), g_0 = |w| (cos, sin) (2), g_1 = g_0 u (4); per target
+        # the packed add and step (4 lanes, 2 instructions; no step for the
+        # first two targets)
+        lanes = 4.0 - 4.0 / V + (9 + 15 + 2 + 4) / V
+        xu = 3.0 / V
+        issue = 2.0 + (-2 + 12 + 17 + 2 + 4) / V
+        return lanes, xu, issue
+    if path == "recurrence-accurate-shared":
+        # the same where a warp's voxels share a spacing other than the step
+        # records' one: the step phasor and the chain coefficient shared by
+        # the warp, 2 cos(theta_d) (1), 3 shuffles, and 1/32 of the owner
+        # lane's work (the step's compensated phase and sincospif, the
+        # coefficient: about 52 operations)
         lanes = 4.0 - 4.0 / V + (9 + 15 + 2 + 4 + 1 + 52.0 / 32) / V
         xu = (3.0 + 3.0 / 32) / V
         issue = 2.0 + (-2 + 12 + 17 + 2 + 4 + 1 + 3 + 55.0 / 32) / V
         return lanes, xu, issue
-    # recurrence (fast mode), V targets per thread, as two chains (even and
-    # odd targets).  Per (thread, sample): the two phases as 3 packed
-    # instructions (6 lane operations), + arg(w) (1), the two reductions
-    # (2 rintf, 2 FADD) and 2 pi t as one packed multiply (2 lanes),
-    # g_0 = |w| (cos, sin) (2), g_1 = g_0 u (4), 2 cos(theta_d) (1),
-    # 2 cos(2 theta_d) (1), 4 sin/cos.  Per target: one packed add into its
-    # accumulator (2 lane operations), and from the third target on one
-    # packed three-term step (2 lane operations; the steps to targets 2 and 3
-    # use 2 cos(theta_d), the rest 2 cos(2 theta_d)).
-    lanes = 4.0 - 4.0 / V + 19.0 / V
-    xu = 6.0 / V
-    issue = (2.0 * V - 2.0 + 3.0 + 1.0 + 2.0 + 2.0 + 1.0 + 4.0 + 2.0 + 4.0 + 1.0 + 1.0) / V
+    if path == "recurrence-per-thread":
+        # fast mode where the warp's voxels do not share the step records'
+        # spacing: per (thread, sample) the two phases as 3 packed
+        # instructions (6 lane operations), + arg(w) (1), the two reductions
+        # (2 rintf, 2 FADD) and 2 pi t as one packed multiply (2 lanes),
+        # g_0 = |w| (cos, sin) (2), g_1 = g_0 u (4), 2 cos(theta_d) (1),
+        # 2 cos(2 theta_d) (1), 4 sin/cos; per target as below
+        lanes = 4.0 - 4.0 / V + 19.0 / V
+        xu = 6.0 / V
+        issue = (2.0 * V - 2.0 + 3.0 + 1.0 + 2.0 + 2.0 + 1.0 + 4.0 + 2.0 + 4.0 + 1.0 + 1.0) / V
+        return lanes, xu, issue
+    # recurrence (fast mode) on an image grid, V targets per thread, as two
+    # chains (even and odd targets), the step phasor u and the chain
+    # coefficients from the tile's step records.  Per (thread, sample): the
+    # anchor's phase with arg(w) (3 FFMA), its reduction (1 rintf, 1 FADD)
+    # and 2 pi t (1), sin and cos, g_0 = |w| (cos, sin) (2), g_1 = g_0 u (4).
+    # Per target: one packed add into its accumulator (2 lane operations),
+    # and from the third target on one packed three-term step (2 lane
+    # operations; the steps to targets 2 and 3 use 2 cos(theta_d), the rest
+    # 2 cos(2 theta_d)).
+    lanes = 4.0 - 4.0 / V + 11.0 / V
+    xu = 3.0 / V
+    issue = (2.0 * V - 2.0 + 3.0 + 1.0 + 1.0 + 1.0 + 2.0 + 2.0 + 4.0) / V
     return lanes, xu, issue
 
 

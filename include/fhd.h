@@ -52,8 +52,11 @@
  *            FHD_MODE_ACCURATE forms each pair's reduced phase from the
  *            three products k_j x_j reduced one by one (error below 2e-7
  *            cycles for any |k.x| < 2^21) and evaluates sin/cos with an
- *            FMA-pipe minimax polynomial (error below 2.4e-7); the step
- *            phasors of the equal-spacing recurrences use sincospif.
+ *            FMA-pipe minimax polynomial (error below 2.4e-7).  The step
+ *            phasors of the equal-spacing recurrences come, on an image grid
+ *            (voxels with one common spacing), from per-sample step records
+ *            evaluated in double precision (both modes), else from sincospif
+ *            per thread.
  *            Relative L2 error against an fp64 evaluation: below 2e-6 on
  *            the benchmark workloads, and within 1e-5 up to |k| = 4096
  *            cycles/FOV on a unit FOV (tested).
@@ -68,8 +71,10 @@
  *            Either may be OR-ed with FHD_MODE_DIRECT, see below.
  * Spacing    where a thread's 32 consecutive targets (voxels for F^H D,
  *            samples for F rho) are exactly equally spaced, as the voxels of a
- *            regular image grid are, the kernel evaluates two phasors per
- *            (thread, source) and reaches the other targets by the recurrence
+ *            regular image grid are, the kernel evaluates one phasor per
+ *            (thread, source), two where the thread's spacing is not the one
+ *            the per-sample step records hold, and reaches the other targets
+ *            by the recurrence
  *            exp(i 2 pi k.(x0 + v d)) = exp(i 2 pi k.x0) exp(i 2 pi k.d)^v,
  *            an exact identity evaluated in fp32 (same tolerances).  Other
  *            targets are evaluated pair by pair.  Likewise, where runs of
@@ -242,7 +247,7 @@ FHD_API fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *t
  * problems return FHD_ERR_TOO_LARGE before anything is launched; N is not
  * limited.
  *
- * Memory: every GPU that loads the library holds the array (about 25 MiB)
+ * Memory: every GPU that loads the library holds the array (about 26 MiB)
  * until the process exits.  The first call on a device, with that device
  * current, looks up the array's device address (cudaGetSymbolAddress) and
  * caches it; make that first call before any stream capture begins.
@@ -256,7 +261,7 @@ FHD_API fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *t
  */
 #define FHD_NOALLOC_MAX_SAMPLES 131072
 #define FHD_NOALLOC_MAX_CTAS 160
-#define FHD_NOALLOC_SCRATCH_BYTES (768 + (size_t)FHD_NOALLOC_MAX_SAMPLES * 33 + \
+#define FHD_NOALLOC_SCRATCH_BYTES (1024 + (size_t)FHD_NOALLOC_MAX_SAMPLES * 49 + \
                                    (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * 8192 * 4)
 FHD_API fhd_status fhd_compute_noalloc(int64_t M, const float *kx, const float *ky, const float *kz,
                                const float *Dr, const float *Di,

@@ -47,6 +47,19 @@ FHD_API fhd_status fhd_test_compute_skip_tile(int64_t M, const float *kx, const 
 FHD_API int fhd_test_set_path(int path);
 
 /*
+ * Turns the adjoint gather's step records on (1, the default) or off (0) for
+ * every later call in this process.  The records hold, per sample, the step
+ * phasor exp(i 2 pi k.d) and the chain coefficients of the target-side
+ * recurrence for the launch's common voxel spacing d, evaluated once in
+ * double precision; without them every thread evaluates its own.  Results
+ * agree within the tolerance of the mode, not bit for bit.  Returns the
+ * previous setting, or -1 (setting unchanged) for any other value.
+ * Process-wide and not ordered with calls running in other threads.  Makes
+ * no CUDA call.
+ */
+FHD_API int fhd_test_set_step_records(int enable);
+
+/*
  * The automatic path choice and split-gather shape for one gather of
  * n_targets targets and n_sources sources (both >= 1) on a device with `sms`
  * SMs running `ctas_max` persistent CTAs, with partial_bytes of partial rows

@@ -65,6 +65,12 @@ Layout layout_for(fhd_op op, int64_t N, int64_t M, int sms) {
     off = align_up(off + (size_t)padded * kRecordBytes, kWsAlign);
     L.desc = off;
     off = align_up(off + (size_t)(padded / kSegment) * 16, kWsAlign);
+    // step records of the adjoint gather, whose sources are the M samples
+    L.steps = 0;
+    if (op != FHD_OP_FWD) {
+        L.steps = off;
+        off = align_up(off + (size_t)(ceil_div(std::max<int64_t>(M, 1), kTile) * kTile) * 16, kWsAlign);
+    }
     L.partial = off;
     off = align_up(off + (size_t)(2 * ctas) * 2 * kTargetsPerBlock * sizeof(float), kWsAlign);
     L.frho = off;
@@ -120,6 +126,8 @@ fhd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FHD_OK : FHD_E
 // Path override for the test-suite (fhd_test_set_path): 0 automatic,
 // 1 always the persistent gather, 2 always the split gather.
 std::atomic<int> g_test_path{0};
+// Step records of the adjoint gather on (1) or off (fhd_test_set_step_records).
+std::atomic<int> g_test_step_records{1};
 
 // Shape of the split gather for n_targets x n_sources, and whether the
 // persistent gather would leave more than half of the device's CTA thread
@@ -207,8 +215,13 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     // polar weights in the adjoint gather (see pack_sources)
     const bool polar = kPolarAdjoint && g.sign > 0.f;
     const int pack_grid = (int)std::min<int64_t>(ceil_div(padded, 256), (int64_t)sms * 8);
+    // step records for the target-side recurrence of the adjoint gather
+    float4* steps = (polar && L.steps != 0 && g_test_step_records.load() != 0)
+                        ? reinterpret_cast<float4*>(ws + L.steps)
+                        : nullptr;
     pack_sources<<<pack_grid, 256, 0, stream>>>(g.sx, g.sy, g.sz, g.wr, g.wi, sign, polar ? 1 : 0, g.n_sources,
-                                                padded, packed, status, first_pass ? 1 : 0, skip);
+                                                padded, packed, g.tx, g.ty, g.tz, g.n_targets, steps, status,
+                                                first_pass ? 1 : 0, skip);
     if ((e = cudaGetLastError()) != cudaSuccess) return FHD_ERR_CUDA;
 
     float4* desc = reinterpret_cast<float4*>(ws + L.desc);
@@ -232,6 +245,7 @@ fhd_status run_gather(const GatherProblem& g, fhd_mode mode, unsigned char* ws, 
     a.tz = g.tz;
     a.packed = packed;
     a.desc = desc;
+    a.steps = steps;
     a.out_r = g.out_r;
     a.out_i = g.out_i;
     a.partial = partial;
@@ -490,6 +504,7 @@ namespace {
 // their own layout.
 constexpr size_t kNoAllocLayoutBytes = kHeaderBytes + (size_t)FHD_NOALLOC_MAX_SAMPLES * kRecordBytes + kWsAlign +
                                        (size_t)FHD_NOALLOC_MAX_SAMPLES / kSegment * 16 + kWsAlign +
+                                       (size_t)FHD_NOALLOC_MAX_SAMPLES * 16 + kWsAlign +
                                        (size_t)FHD_NOALLOC_MAX_CTAS * 2 * 2 * kTargetsPerBlock * sizeof(float);
 constexpr size_t kNoAllocScratchBytes =
     FHD_NOALLOC_SCRATCH_BYTES > kNoAllocLayoutBytes ? FHD_NOALLOC_SCRATCH_BYTES : kNoAllocLayoutBytes;
@@ -611,6 +626,12 @@ fhd_status fhd_test_check_array(const void* p, size_t bytes, int device) {
 int fhd_test_set_path(int path) {
     if (path < 0 || path > 2) return -1;
     return g_test_path.exchange(path);
+}
+
+// Declared in include/fhd_testing.h.
+int fhd_test_set_step_records(int enable) {
+    if (enable != 0 && enable != 1) return -1;
+    return g_test_step_records.exchange(enable);
 }
 
 // Declared in include/fhd_testing.h.

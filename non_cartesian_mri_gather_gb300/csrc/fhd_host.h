@@ -28,6 +28,7 @@ inline bool fast_mode(fhd_mode m) { return ((int)m & FHD_MODE_FAST) != 0; }
 struct Layout {
     size_t packed;   // offset of packed source records
     size_t desc;     // offset of the per-segment descriptors of the packed records
+    size_t steps;    // offset of the adjoint gather's step records (0: none, the forward-only layout)
     size_t partial;  // offset of per-CTA partial slots
     size_t frho;     // offset of F rho (fhfrho_apply only)
     size_t total;

@@ -72,7 +72,7 @@ namespace fhd {
 #define FHD_TILE 256
 #endif
 #ifndef FHD_STAGES
-#define FHD_STAGES 6
+#define FHD_STAGES 5
 #endif
 #ifndef FHD_MIN_CTAS_PER_SM
 #define FHD_MIN_CTAS_PER_SM 1
@@ -89,6 +89,12 @@ namespace fhd {
 #ifndef FHD_HORNER_GROUP
 #define FHD_HORNER_GROUP 8
 #endif
+#ifndef FHD_UNROLL_PRE
+#define FHD_UNROLL_PRE 6
+#endif
+#ifndef FHD_UNROLL_PRE_ACCURATE
+#define FHD_UNROLL_PRE_ACCURATE 4
+#endif
 
 constexpr int kThreads = FHD_THREADS;    // consumer threads per CTA
 constexpr int kWarps = kThreads / 32;    // consumer warps
@@ -98,6 +104,7 @@ constexpr int kTile = FHD_TILE;          // sources per staged tile
 constexpr int kStages = FHD_STAGES;      // shared-memory ring depth
 constexpr int kRecordBytes = 32;         // one packed source
 constexpr int kTileBytes = kTile * kRecordBytes;
+constexpr int kStepBytes = kTile * 16;   // one step record (float4) per source
 // Source segments: kSegment consecutive packed sources (fast mode; accurate
 // mode's length is set below) whose coordinates are exactly equally spaced
 // take the source-side path; one 16-byte descriptor {step.x, step.y,
@@ -115,6 +122,9 @@ constexpr int kUnrollSharedU = 12;       // the same in the accurate warp-shared
 // forward kernel)
 constexpr int kUnrollTwoChains = 6;
 constexpr int kUnrollOneChain = 3;
+// the same with the staged step records (accumulate_tile_pre), per mode
+constexpr int kUnrollPreFast = FHD_UNROLL_PRE;
+constexpr int kUnrollPreAccurate = FHD_UNROLL_PRE_ACCURATE;
 // The adjoint gathers store each weight in polar form, {|w|, arg(w) / 2 pi}
 // (see pack_sources); the forward gathers, whose voxel weights Horner's rule
 // adds as complex numbers, keep {w.re, w.im}.
@@ -220,6 +230,7 @@ struct GatherArgs {
     const float* __restrict__ tz;
     const float4* __restrict__ packed;  // n_tiles * kTile records of 2 float4
     const float4* __restrict__ desc;    // n_tiles * (kTile / SEG) segment descriptors
+    const float4* __restrict__ steps;   // n_tiles * kTile step records, or nullptr (see pack_sources)
     float* __restrict__ out_r;
     float* __restrict__ out_i;
     float* __restrict__ partial;    // [2*ctas slots][2][kTargetsPerBlock]
@@ -409,6 +420,14 @@ __device__ __forceinline__ float two_cos_double(float s, float c) {
 }
 
 // ---------------------------------------------------------------- pack
+// The launch's common target spacing along one axis: the float32 value of
+// t[1] - t[0], the difference formed in double exactly as the gather's
+// per-thread spacing check (equally_spaced) forms it, so the two agree bit
+// for bit; 0 with fewer than two targets.
+__device__ __forceinline__ float launch_step(const float* __restrict__ t, int64_t n) {
+    return n >= 2 ? (float)((double)t[1] - (double)t[0]) : 0.f;
+}
+
 // Source records {A.x, A.x, A.y, A.y, A.z, A.z, w.re, w.im} with A = sign*a
 // (exact; sign is -1 for the forward sum, whose sources are the voxels, and +1
 // for the adjoint sum; phases are in cycles in both modes): each coordinate
@@ -420,20 +439,39 @@ __device__ __forceinline__ float two_cos_double(float s, float c) {
 // the phase becomes an FMA) and the complex multiply-accumulate of a pair
 // becomes two real ones.
 // Records n..n_padded-1 are zero (weight 0, so they add exactly 0).
+//
+// With `steps`, the kernel also writes one step record per source for the
+// launch's common target spacing d (launch_step): {cos theta, sin theta,
+// 2 cos theta, 2 cos 2 theta} with theta = 2 pi A.d, each evaluated in double
+// (the three products of float32 values are exact there, the phase is
+// reduced by its nearest integer before sincospi, and 2 cos 2 theta =
+// 2 (cos theta - sin theta)(cos theta + sin theta)) and rounded once.  These
+// are the step phasor u and the two chain coefficients of the target-side
+// recurrence; on an image grid every thread's spacing is d, so the gather
+// reads them instead of evaluating them per thread.  Padding records are zero.
+//
 // With `reset_status`, block 0 thread 0 also clears the status word (stream
 // order puts this before the gather kernel); the second pass of F^H F rho
 // keeps the word so a timeout of the first pass stays visible.
 __global__ void pack_sources(const float* __restrict__ ax, const float* __restrict__ ay,
                              const float* __restrict__ az, const float* __restrict__ wr,
                              const float* __restrict__ wi, float sign, int polar, int64_t n, int64_t n_padded,
-                             float4* __restrict__ out, uint32_t* status, int reset_status,
-                             const uint32_t* skip) {
+                             float4* __restrict__ out, const float* __restrict__ tx, const float* __restrict__ ty,
+                             const float* __restrict__ tz, int64_t n_targets, float4* __restrict__ steps,
+                             uint32_t* status, int reset_status, const uint32_t* skip) {
     if (skip != nullptr && *skip != 0u) return;
     if (reset_status && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+    double dx = 0.0, dy = 0.0, dz = 0.0;
+    if (steps != nullptr) {
+        dx = launch_step(tx, n_targets);
+        dy = launch_step(ty, n_targets);
+        dz = launch_step(tz, n_targets);
+    }
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_padded;
          i += (int64_t)gridDim.x * blockDim.x) {
         float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f);
         float4 r1 = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < n) {
             const float X = sign * ax[i], Y = sign * ay[i], Z = sign * az[i];
             r0 = make_float4(X, X, Y, Y);
@@ -443,9 +481,17 @@ __global__ void pack_sources(const float* __restrict__ ax, const float* __restri
             } else {
                 r1 = make_float4(Z, Z, wr[i], wi[i]);
             }
+            if (steps != nullptr) {
+                const double p = (double)X * dx + (double)Y * dy + (double)Z * dz;
+                const double t = p - rint(p);
+                double su, cu;
+                sincospi(2.0 * t, &su, &cu);
+                q = make_float4((float)cu, (float)su, (float)(2.0 * cu), (float)(2.0 * (cu - su) * (cu + su)));
+            }
         }
         out[2 * i] = r0;
         out[2 * i + 1] = r1;
+        if (steps != nullptr) steps[i] = q;
     }
 }
 
@@ -481,6 +527,9 @@ __global__ void describe_segments(const float* __restrict__ ax, const float* __r
 struct __align__(16) GatherSmem {
     float4 ring[kStages][kTile * 2];
     float4 desc[kStages][kSegmentsPerTile];
+    // The tile's step records (pack_sources), staged with it when the launch
+    // has them.
+    float4 step[kStages][kTile];
     // Running sums of the current segment, one private column per consumer
     // thread (rows: kV real parts, then kV imaginary parts).  They are touched
     // once per tile, so keeping them here instead of in registers frees
@@ -903,14 +952,73 @@ __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* _
     }
 }
 
+// Every thread of the warp with the launch's common target spacing d, and the
+// tile's step records staged beside it (pack_sources: u = exp(i 2 pi a_s.d)
+// and the chain coefficients 2 cos theta_d, 2 cos 2 theta_d, each from
+// double precision): the thread evaluates only its anchor phasor per source,
+// then the two chains of accumulate_tile_strided.  Polar records only (the
+// adjoint gathers).
+template <int MODE>
+__device__ __forceinline__ void accumulate_tile_pre(const float4* __restrict__ rec, const float4* __restrict__ step,
+                                                    float x0, float y0, float z0, f2_t (&acc)[kV]) {
+#pragma unroll
+    for (int v = 0; v < kV; ++v) acc[v] = 0ull;  // +0.0f in both halves
+    constexpr int kU = MODE == kAccurate ? kUnrollPreAccurate : kUnrollPreFast;
+#pragma unroll kU
+    for (int s = 0; s < kTile; ++s) {
+        const float4 r0 = rec[2 * s];      // A.x A.x A.y A.y
+        const float4 r1 = rec[2 * s + 1];  // A.z A.z |w| phi
+        const float4 q = step[s];          // cos theta_d, sin theta_d, 2 cos theta_d, 2 cos 2 theta_d
+        float s0, c0;
+        if constexpr (MODE == kAccurate) {
+            phasor_accurate_off(r1.w, r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
+        } else {
+            // phase in cycles, the weight's phase first, reduced to
+            // 2 pi (p - rint(p)) for the hardware sin/cos
+            const float p0 = fmaf(r1.x, z0, fmaf(r0.z, y0, fmaf(r0.x, x0, r1.w)));
+            const float th0 = (p0 - rintf(p0)) * kTwoPi;
+            s0 = __sinf(th0);
+            c0 = __cosf(th0);
+        }
+        const float fr = r1.z * c0;  // g_0 = |w| exp(i 2 pi (a.b_0 + phi))
+        const float fi = r1.z * s0;
+        const float gr = fmaf(fr, q.x, -fi * q.y);  // g_1 = g_0 u
+        const float gi = fmaf(fr, q.y, fi * q.x);
+        const f2_t e0 = f2_pack(fr, fi), e1 = f2_pack(gr, gi);
+        const f2_t e2n = f2_fma(f2_pack(-q.z, -q.z), e1, e0);  // -e_2
+        const f2_t e3n = f2_fma(f2_pack(q.z, q.z), e2n, e1);   // -e_3
+        const f2_t kposC = f2_pack(q.w, q.w), knegC = f2_pack(-q.w, -q.w);
+        f2_t amA = e0, aA = e2n, amB = e1, aB = e3n;  // chains over even and odd targets
+        acc[0] = f2_add(acc[0], e0);
+        acc[1] = f2_add(acc[1], e1);
+        acc[2] = f2_add(acc[2], e2n);
+        acc[3] = f2_add(acc[3], e3n);
+#pragma unroll
+        for (int j = 1; 2 * j + 3 < kV; ++j) {
+            const f2_t nA = f2_fma((j & 1) ? kposC : knegC, aA, amA);  // s_{j+1} a_{j+1}
+            const f2_t nB = f2_fma((j & 1) ? kposC : knegC, aB, amB);
+            amA = aA;
+            aA = nA;
+            amB = aB;
+            aB = nB;
+            acc[2 * j + 2] = f2_add(acc[2 * j + 2], aA);
+            acc[2 * j + 3] = f2_add(acc[2 * j + 3], aB);
+        }
+    }
+}
+
 // One staged tile on the target-side recurrence, folded into the thread's
-// running sums (the signs of the stored terms undone here).
+// running sums (the signs of the stored terms undone here).  `step`: the
+// tile's step records when the warp takes accumulate_tile_pre, else nullptr.
 template <int MODE, bool TWO, bool POLAR>
 __device__ __forceinline__ void strided_tile(const float4* __restrict__ rec, float x0, float y0, float z0,
                                              float dx, float dy, float dz, int lane, bool shared_u,
-                                             float (*run)[kThreads], int tid) {
+                                             const float4* __restrict__ step, float (*run)[kThreads], int tid) {
+    static_assert(TWO || !POLAR, "the adjoint gathers run two chains");
     f2_t acc[kV];
-    if constexpr (MODE == kAccurate) {
+    if (POLAR && step != nullptr) {
+        if constexpr (POLAR) accumulate_tile_pre<MODE>(rec, step, x0, y0, z0, acc);
+    } else if constexpr (MODE == kAccurate) {
         if (shared_u)
             accumulate_tile_strided_shared_u<MODE, POLAR>(rec, x0, y0, z0, dx, dy, dz, lane, acc);
         else
@@ -1247,8 +1355,16 @@ __device__ __noinline__ void accumulate_tile_src_strided_ool(const float4* __res
 // kSegmentAccurate for the forward gather).  POLAR: the records hold polar
 // weights (the adjoint gather; see pack_sources).  Each combination in use is
 // its own instantiation.
+// FHD_GATHER_MAXNREG, when defined, sets the kernel's register cap directly
+// (a 288-thread CTA fits up to 224 registers a thread); by default the launch
+// bounds set it.
+#ifdef FHD_GATHER_MAXNREG
+#define FHD_GATHER_BOUNDS __maxnreg__(FHD_GATHER_MAXNREG)
+#else
+#define FHD_GATHER_BOUNDS __launch_bounds__(kCtaThreads, kMinCtasPerSm)
+#endif
 template <int MODE, int NPOLY, int SEG, bool POLAR>
-__global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(const GatherArgs args) {
+__global__ void FHD_GATHER_BOUNDS gather_kernel(const GatherArgs args) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // The target-side recurrence runs as two chains (even and odd targets),
     // except in the fast forward gather, where a single chain measured faster
@@ -1266,6 +1382,8 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
     const int64_t w_end = sch.start(c + 1);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // step records: only the adjoint gathers' target-side recurrence uses them
+    const bool with_steps = POLAR && args.steps != nullptr;
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < kStages; ++st) {
@@ -1292,9 +1410,10 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
             if (w == args.skip_tile) continue;  // test hook: this copy never arrives
             const int64_t j = w % sch.n_tiles;
             constexpr int kTileDescBytes = kTile / SEG * 16;
-            mbar_arrive_expect_tx(&sm.full[st], kTileBytes + kTileDescBytes);
+            mbar_arrive_expect_tx(&sm.full[st], kTileBytes + kTileDescBytes + (with_steps ? kStepBytes : 0));
             bulk_copy_g2s(&sm.ring[st][0], args.packed + j * (kTile * 2), kTileBytes, &sm.full[st]);
             bulk_copy_g2s(&sm.desc[st][0], args.desc + j * (kTile / SEG), kTileDescBytes, &sm.full[st]);
+            if (with_steps) bulk_copy_g2s(&sm.step[st][0], args.steps + j * kTile, kStepBytes, &sm.full[st]);
         }
         // Drain: the last copy issued into each stage must have landed before
         // this CTA's shared memory can be released.
@@ -1315,6 +1434,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
     float sx = 0.f, sy = 0.f, sz = 0.f;  // target spacing of the strided path
     bool strided = false;                // warp-uniform
     bool shared_u = false;               // strided, and every lane has the same spacing
+    bool pre = false;                    // strided, and every lane has the launch's common spacing
     const int tid = threadIdx.x;
     int64_t seg_first_tile = 0;  // first tile index of the current segment
     int64_t consumed = 0;
@@ -1356,6 +1476,12 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
             const bool same_step = __all_sync(0xffffffffu, sx == sx0 && sy == sy0 && sz == sz0);
             strided = args.allow_strided && all_spaced;
             shared_u = strided && same_step;
+            // the spacing the step records were evaluated for (pack_sources);
+            // a thread with fewer than two targets has any spacing
+            const bool common = with_steps && (n_in < 2 || (sx == launch_step(args.tx, sch.n_targets) &&
+                                                             sy == launch_step(args.ty, sch.n_targets) &&
+                                                             sz == launch_step(args.tz, sch.n_targets)));
+            pre = strided && __all_sync(0xffffffffu, common);
         }
 
         const int st = (int)(consumed % kStages);
@@ -1369,10 +1495,13 @@ __global__ void __launch_bounds__(kCtaThreads, kMinCtasPerSm) gather_kernel(cons
         const float4* rec = &sm.ring[st][0];
         if (strided) {
             if constexpr (MODE == kFast) {
-                strided_tile<MODE, kTwoChains, POLAR>(rec, x0, y0, z0, sx, sy, sz, lane, shared_u, sm.run, tid);
+                strided_tile<MODE, kTwoChains, POLAR>(rec, x0, y0, z0, sx, sy, sz, lane, shared_u,
+                                                      pre ? &sm.step[st][0] : nullptr, sm.run, tid);
             } else {
                 f2_t acc[kV];
-                if (shared_u)
+                if (POLAR && pre) {
+                    if constexpr (POLAR) accumulate_tile_pre<MODE>(rec, &sm.step[st][0], x0, y0, z0, acc);
+                } else if (shared_u)
                     accumulate_tile_strided_shared_u<MODE, POLAR>(rec, x0, y0, z0, sx, sy, sz, lane, acc);
                 else
                     accumulate_tile_strided<MODE, kTwoChains, POLAR>(rec, x0, y0, z0, sx, sy, sz, acc);

@@ -101,6 +101,27 @@ def gpu_fhf(p, mode):
 PATH_AUTO, PATH_PERSISTENT, PATH_SPLIT = 0, 1, 2
 
 
+class step_records:
+    """Context manager: turn the adjoint gather's step records on or off
+    (fhd_test_set_step_records)."""
+
+    def __init__(self, enable: int):
+        self.enable = enable
+
+    def __enter__(self):
+        import non_cartesian_mri_gather_gb300 as fhd
+
+        self.prev = fhd.load().fhd_test_set_step_records(self.enable)
+        assert self.prev in (0, 1)
+        return self
+
+    def __exit__(self, *exc):
+        import non_cartesian_mri_gather_gb300 as fhd
+
+        fhd.load().fhd_test_set_step_records(self.prev)
+        return False
+
+
 class gather_path:
     """Context manager: force the library's gather path (fhd_test_set_path)."""
 

@@ -143,6 +143,11 @@ def test_set_path_hook(lib):
     assert lib.fhd_test_set_path(-1) == -1
     assert lib.fhd_test_set_path(2) == 0
     assert lib.fhd_test_set_path(prev) == 2
+    prev = lib.fhd_test_set_step_records(1)
+    assert prev in (0, 1)
+    assert lib.fhd_test_set_step_records(2) == -1
+    assert lib.fhd_test_set_step_records(0) == 1
+    assert lib.fhd_test_set_step_records(prev) == 0
 
 
 # Partial rows of a workspace on a 152-SM device: 2 slots per CTA of

@@ -32,20 +32,28 @@ def test_roofline_counts():
     assert (lanes, xu, issue) == (5 + (4 * 6 + 12 * 2) / 8, 2 * 6 / 8, 61 / 8)
     assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct") - 152 * (16 / xu) * 2070e6) < 1
     assert 16 / xu < min(128 / lanes, 128 / issue)
-    # the recurrence: per target 4 lanes in 2 instructions (the first two
-    # targets take no step), per (thread, sample) 19 lanes, 6 operations on
-    # the 16-lane pipe (4 sin/cos, 2 rintf) and 21 instructions
+    # the recurrence with step records: per target 4 lanes in 2 instructions
+    # (the first two targets take no step), per (thread, sample) 11 lanes
+    # (the anchor's phase 3, reduction 1, 2 pi t 1, g_0 2, g_1 4), 3
+    # operations on the 16-lane pipe (sin, cos, rintf) and 14 instructions
     lanes, xu, issue = bench.per_pair_counts("recurrence")
     V = bench.TARGETS_PER_THREAD
-    assert abs(lanes - (4 - 4 / V + 19 / V)) < 1e-12 and abs(xu - 6 / V) < 1e-12
-    assert abs(issue - (2 + 19 / V)) < 1e-12
+    assert abs(lanes - (4 - 4 / V + 11 / V)) < 1e-12 and abs(xu - 3 / V) < 1e-12
+    assert abs(issue - (2 + 12 / V)) < 1e-12
+    # a warp evaluating its own step phasor: 19 lanes, 6 on the 16-lane pipe
+    # (4 sin/cos, 2 rintf) and 21 instructions per (thread, sample)
+    lanes_t, xu_t, issue_t = bench.per_pair_counts("recurrence-per-thread")
+    assert abs(lanes_t - (4 - 4 / V + 19 / V)) < 1e-12 and abs(xu_t - 6 / V) < 1e-12
+    assert abs(issue_t - (2 + 19 / V)) < 1e-12
     # with V = 32 the FP32 lanes bind
     assert abs(bench.peak_pairs_per_s(152, 2070.0, "recurrence") - 152 * (128 / lanes) * 2070e6) < 1
     # accurate pair by pair: 26 FP32 lane operations per pair bind
     lanes, xu, issue = bench.per_pair_counts("direct-accurate")
     assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct-accurate") - 152 * (128 / lanes) * 2070e6) < 1
-    for path in ("source", "recurrence-accurate"):
+    for path in ("source", "recurrence-accurate", "recurrence-accurate-shared"):
         assert all(v > 0 for v in bench.per_pair_counts(path))
+    # the step records take work off the accurate recurrence too
+    assert bench.per_pair_counts("recurrence-accurate")[0] < bench.per_pair_counts("recurrence-accurate-shared")[0]
 
 
 def test_profiled_traffic_is_guarded():

@@ -218,7 +218,7 @@ def test_launch_shape():
     for mode in (0, 1, 2, 3):
         shape = fhd.fhd_launch_shape(0, mode)
         assert shape["ctas"] == sms
-        assert (shape["threads"], shape["targets_per_thread"], shape["tile_sources"], shape["stages"]) == (256, 32, 256, 6)
+        assert (shape["threads"], shape["targets_per_thread"], shape["tile_sources"], shape["stages"]) == (256, 32, 256, 5)
     lib = fhd.load()
     vals = [ctypes.c_int(0) for _ in range(5)]
     assert lib.fhd_launch_shape(0, 4, *(ctypes.addressof(v) for v in vals)) == 1  # unknown mode bit

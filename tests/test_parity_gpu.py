@@ -23,7 +23,8 @@ import pytest
 import oracle
 from inputs import make_workload, random_problem
 from tests.gpu_helpers import (PATH_AUTO, PATH_PERSISTENT, PSNR_FAST_DB, TOL_ACCURATE, TOL_FAST, gather_path, gpu_fhd,
-                               gpu_fhf, gpu_fwd, psnr_db, rel_l2, rel_l2_by_position, sample_indices)
+                               gpu_fhf, gpu_fwd, psnr_db, rel_l2, rel_l2_by_position, sample_indices,
+                               step_records)
 
 pytestmark = pytest.mark.gpu
 
@@ -258,16 +259,24 @@ def test_fhd_small_grid_rows(N, M, mode):
 
 @pytest.mark.parametrize("mode", ALL_MODES)
 def test_rows_with_mixed_spacing(mode):
-    """Rows of 32 voxels, each one thread's targets, whose x spacing alternates
-    between 1/32 and 1/64 every 16 rows: every thread is equally spaced but a
-    warp's lanes differ in spacing, so the accurate recurrence evaluates the
-    step phasor per thread instead of once per warp (warps with a single
-    spacing follow further on)."""
-    rows = 320
+    """Rows of 32 voxels, each one thread's targets (a warp holds 32 rows).
+    Every thread is equally spaced, and the launch's common spacing (that of
+    its first two voxels) is 1/32:
+    - rows 0-255 alternate between 1/32 and 1/64 every 16 rows, so a warp's
+      lanes differ in spacing and each thread evaluates its own step phasor;
+    - rows 256-319 (two warps) all have 1/32 and read the step records that
+      the pack kernel evaluated for it;
+    - rows 320-383 (two warps) all have 1/64: one spacing per warp, but not
+      the records' one (the accurate kernel shares one lane's step phasor
+      across the warp)."""
+    rows = 384
     i = np.arange(32)
     xs = []
     for r in range(rows):
-        step = 1 / 32 if (r // 16) % 2 == 0 or r >= 256 else 1 / 64
+        if r >= 320:
+            step = 1 / 64
+        else:
+            step = 1 / 32 if (r // 16) % 2 == 0 or r >= 256 else 1 / 64
         xs.append(-0.5 + i * step)
     p = random_problem(32 * rows, 900, kmax=16.0, seed=14)
     p.x = np.concatenate(xs).astype(np.float32)
@@ -286,6 +295,26 @@ def test_perturbed_grid_falls_back(mode):
     p.x[3001] = np.nextafter(p.x[3001], np.float32(1.0))
     ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
     check(gpu_fhd(p, mode), ref, mode, "F^H D perturbed grid")
+
+
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_step_records_differ_but_both_match(mode):
+    """The adjoint gather's step records (the recurrence's step phasor and
+    chain coefficients for the launch's voxel spacing, evaluated once per
+    sample in double) against every thread evaluating its own: both match
+    the oracle, at every position of a thread's run, and the results are not
+    bit-identical, so the records were read."""
+    p = random_problem(32768, 2000, kmax=32.0, seed=16, coords="grid")  # a 32^3 grid
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    a = gpu_fhd(p, mode)
+    with step_records(0):
+        b = gpu_fhd(p, mode)
+    tol = TOL_ACCURATE if mode == ACC else TOL_FAST
+    for got, what in ((a, "step records"), (b, "per-thread steps")):
+        check(got, ref, mode, what)
+        worst = max(rel_l2_by_position(got, ref, np.arange(p.N)).values())
+        assert worst <= tol, f"{what}: worst position relL2 {worst:.3e}"
+    assert not np.array_equal(a, b), "the step records were not used"
 
 
 def test_recurrence_and_direct_differ_but_both_match():
