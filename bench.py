@@ -307,6 +307,17 @@ def peak_pairs_per_s(sms: int, mhz: float, path: str = "direct") -> float:
     return sms * per_clk * mhz * 1e6
 
 
+def fp32_probe(fhd, device: int):
+    """FP32 lane operations per second of the library's packed-FMA probe
+    kernel on `device` (fhd_test_fma2_rate), or None if it failed."""
+    import ctypes
+
+    rate = ctypes.c_double(0.0)
+    if fhd.load().fhd_test_fma2_rate(device, ctypes.byref(rate)) != 0 or rate.value <= 0:
+        return None
+    return rate.value
+
+
 KERNEL_SOURCES = ("non_cartesian_mri_gather_gb300/csrc/fhd_kernels.cuh",
                   "non_cartesian_mri_gather_gb300/csrc/sincos_poly.cuh",
                   "non_cartesian_mri_gather_gb300/csrc/fhd_api.cu")
@@ -680,6 +691,17 @@ def run_ours(args, world, rank, local):
         roof["frac_at_sampled_clock"] = achieved / peak_pairs_per_s(sms, clk["sm_mhz"], path)
     if fhf and not args.mode.startswith("fast"):
         roof["peak_basis"] += " (the fast mode's operation counts: an upper bound for accurate mode)"
+    # ---- the packed FP32 rate this GPU reaches in practice (a register-only
+    # probe kernel, after the timed region): the gather's FP32 lane operations
+    # per second, from the same per-pair count as the bound, as a share of it
+    probe = fp32_probe(fhd, torch.cuda.current_device())
+    if probe:
+        lanes_per_pair = ((per_pair_counts("source")[0] + per_pair_counts("recurrence")[0]) / 2 if fhf
+                          else n_fma)
+        lanes = achieved * lanes_per_pair
+        roof["fp32_probe"] = {"lane_ops_per_s": probe, "frac_of_nominal": probe / (sms * FMA_LANES_PER_SM *
+                                                                                   max_mhz * 1e6),
+                              "gather_lane_ops_per_s": lanes, "gather_frac_of_probe": lanes / probe}
 
     # ---- secondary: the accurate pair-by-pair path on the same workload (the
     # path a caller with non-grid voxels takes in accurate mode), a few steps

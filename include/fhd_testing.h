@@ -4,7 +4,8 @@
  * Not part of the operator API in fhd.h; they exist so the test-suite can
  * exercise the bounded-wait failure path without faulting or hanging a GPU,
  * force or inspect the gather path, replay the schedule on the host, check
- * pointers without launching, and check the per-pair phasor on its own.
+ * pointers without launching, check the per-pair phasor on its own, and
+ * measure the device's packed FP32 rate.
  * The library has no counterpart of these on the pages it implements.
  */
 #ifndef FHD_TESTING_H
@@ -58,6 +59,20 @@ FHD_API int fhd_test_set_path(int path);
  * no CUDA call.
  */
 FHD_API int fhd_test_set_step_records(int enable);
+
+/*
+ * The packed FP32 rate this device reaches in practice, in FP32 lane
+ * operations per second (an FMA counts as one per lane, a packed FMA as two):
+ * one CTA of 256 threads per SM, each stepping 16 independent chains of
+ * packed f32x2 FMAs (x = x * m + a) in registers, timed with CUDA events on
+ * the legacy default stream of `device` after one warm-up launch (a few
+ * milliseconds in all).  The gather kernels' bound counts FP32 lane
+ * operations against the nominal 128 per SM per clock; this is the same unit
+ * as the hardware delivers it to a kernel that does nothing else.
+ * Synchronises the device's legacy default stream.  Returns FHD_ERR_CUDA on
+ * any CUDA error (and *lane_ops_per_s = 0).
+ */
+FHD_API fhd_status fhd_test_fma2_rate(int device, double *lane_ops_per_s);
 
 /*
  * The automatic path choice and split-gather shape for one gather of

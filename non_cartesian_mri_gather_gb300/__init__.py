@@ -100,6 +100,7 @@ SIGNATURES = {
     "fhd_test_schedule": (_int, [_i64, _i64, _int]),
     "fhd_test_set_path": (_int, [_int]),
     "fhd_test_set_step_records": (_int, [_int]),
+    "fhd_test_fma2_rate": (_int, [_int, ctypes.POINTER(ctypes.c_double)]),
     "fhd_test_split_shape": (_int, [_i64, _i64, _int, _int, _sz, ctypes.POINTER(ctypes.c_int),
                                     ctypes.POINTER(ctypes.c_int64)]),
     "fhd_test_check_array": (_int, [_vp, _sz, _int]),

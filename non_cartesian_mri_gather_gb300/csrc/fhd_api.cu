@@ -584,10 +584,66 @@ __global__ void test_phasor_kernel(int which, int64_t n, const float* __restrict
     }
 }
 
+// fhd_test_fma2_rate: each thread steps kProbeChains independent packed
+// chains x = x * m + a (fma.rn.f32x2) kProbeIters times, the work held in
+// registers; 8 warps per CTA, two per scheduler as in the gather's consumers.
+constexpr int kProbeThreads = 256;
+constexpr int kProbeChains = 16;
+constexpr int kProbeIters = 16384;
+__device__ float g_probe_sink;
+
+__global__ void __launch_bounds__(kProbeThreads, 1) fma2_probe_kernel(float m0) {
+    f2_t x[kProbeChains];
+    const f2_t m = f2_pack(m0, m0), a = f2_pack(1e-7f, 2e-7f);
+#pragma unroll
+    for (int k = 0; k < kProbeChains; ++k) x[k] = f2_pack(threadIdx.x * 1e-3f + k, 0.5f * k);
+#pragma unroll 1
+    for (int i = 0; i < kProbeIters; ++i) {
+#pragma unroll
+        for (int k = 0; k < kProbeChains; ++k) x[k] = f2_fma(x[k], m, a);
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < kProbeChains; ++k) {
+        float lo, hi;
+        f2_unpack(x[k], lo, hi);
+        s += lo + hi;
+    }
+    if (s == -1.0f) g_probe_sink = s;  // never true; keeps the chains live
+}
+
 }  // namespace
 }  // namespace fhd
 
 extern "C" {
+
+// Declared in include/fhd_testing.h.
+fhd_status fhd_test_fma2_rate(int device, double* lane_ops_per_s) {
+    if (lane_ops_per_s == nullptr) return FHD_ERR_INVALID_VALUE;
+    *lane_ops_per_s = 0.0;
+    int prev = 0, sms = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) return FHD_ERR_CUDA;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess) e = cudaEventCreate(&e0);
+    if (e == cudaSuccess) e = cudaEventCreate(&e1);
+    float ms = 0.f;
+    if (e == cudaSuccess) {
+        fma2_probe_kernel<<<sms, kProbeThreads>>>(0.999f);  // warm-up
+        cudaEventRecord(e0);
+        fma2_probe_kernel<<<sms, kProbeThreads>>>(0.999f);
+        cudaEventRecord(e1);
+        e = cudaEventSynchronize(e1);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaSetDevice(prev);
+    if (e != cudaSuccess || ms <= 0.f) return FHD_ERR_CUDA;
+    *lane_ops_per_s = (double)sms * kProbeThreads * kProbeIters * kProbeChains * 2.0 / (ms * 1e-3);
+    return FHD_OK;
+}
 
 // Declared in include/fhd_testing.h.
 fhd_status fhd_test_phasor(int which, int64_t n, const float* ax, const float* ay, const float* az, const float* bx,

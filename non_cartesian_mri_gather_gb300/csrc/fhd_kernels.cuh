@@ -958,6 +958,57 @@ __device__ __forceinline__ void accumulate_tile_strided_shared_u(const float4* _
 // double precision): the thread evaluates only its anchor phasor per source,
 // then the two chains of accumulate_tile_strided.  Polar records only (the
 // adjoint gathers).
+//
+// The anchor phasor exp(i 2 pi (a_s.b_0 + phi_s)) of source s.
+template <int MODE>
+__device__ __forceinline__ void pre_anchor(const float4* __restrict__ rec, int s, float x0, float y0, float z0,
+                                           float& s0, float& c0) {
+    const float4 r0 = rec[2 * s];      // A.x A.x A.y A.y
+    const float4 r1 = rec[2 * s + 1];  // A.z A.z |w| phi
+    if constexpr (MODE == kAccurate) {
+        phasor_accurate_off(r1.w, r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
+    } else {
+        // phase in cycles, the weight's phase first, reduced to
+        // 2 pi (p - rint(p)) for the hardware sin/cos
+        const float p0 = fmaf(r1.x, z0, fmaf(r0.z, y0, fmaf(r0.x, x0, r1.w)));
+        const float th0 = (p0 - rintf(p0)) * kTwoPi;
+        s0 = __sinf(th0);
+        c0 = __cosf(th0);
+    }
+}
+
+// Source s's terms for the thread's kV targets, from its anchor phasor
+// (c0, s0) and its step record, added into acc.
+__device__ __forceinline__ void pre_chains(const float4* __restrict__ rec, const float4* __restrict__ step, int s,
+                                           float s0, float c0, f2_t (&acc)[kV]) {
+    const float w = rec[2 * s + 1].z;  // |w|
+    const float4 q = step[s];          // cos theta_d, sin theta_d, 2 cos theta_d, 2 cos 2 theta_d
+    const float fr = w * c0;           // g_0 = |w| exp(i 2 pi (a.b_0 + phi))
+    const float fi = w * s0;
+    const float gr = fmaf(fr, q.x, -fi * q.y);  // g_1 = g_0 u
+    const float gi = fmaf(fr, q.y, fi * q.x);
+    const f2_t e0 = f2_pack(fr, fi), e1 = f2_pack(gr, gi);
+    const f2_t e2n = f2_fma(f2_pack(-q.z, -q.z), e1, e0);  // -e_2
+    const f2_t e3n = f2_fma(f2_pack(q.z, q.z), e2n, e1);   // -e_3
+    const f2_t kposC = f2_pack(q.w, q.w), knegC = f2_pack(-q.w, -q.w);
+    f2_t amA = e0, aA = e2n, amB = e1, aB = e3n;  // chains over even and odd targets
+    acc[0] = f2_add(acc[0], e0);
+    acc[1] = f2_add(acc[1], e1);
+    acc[2] = f2_add(acc[2], e2n);
+    acc[3] = f2_add(acc[3], e3n);
+#pragma unroll
+    for (int j = 1; 2 * j + 3 < kV; ++j) {
+        const f2_t nA = f2_fma((j & 1) ? kposC : knegC, aA, amA);  // s_{j+1} a_{j+1}
+        const f2_t nB = f2_fma((j & 1) ? kposC : knegC, aB, amB);
+        amA = aA;
+        aA = nA;
+        amB = aB;
+        aB = nB;
+        acc[2 * j + 2] = f2_add(acc[2 * j + 2], aA);
+        acc[2 * j + 3] = f2_add(acc[2 * j + 3], aB);
+    }
+}
+
 template <int MODE>
 __device__ __forceinline__ void accumulate_tile_pre(const float4* __restrict__ rec, const float4* __restrict__ step,
                                                     float x0, float y0, float z0, f2_t (&acc)[kV]) {
@@ -966,44 +1017,9 @@ __device__ __forceinline__ void accumulate_tile_pre(const float4* __restrict__ r
     constexpr int kU = MODE == kAccurate ? kUnrollPreAccurate : kUnrollPreFast;
 #pragma unroll kU
     for (int s = 0; s < kTile; ++s) {
-        const float4 r0 = rec[2 * s];      // A.x A.x A.y A.y
-        const float4 r1 = rec[2 * s + 1];  // A.z A.z |w| phi
-        const float4 q = step[s];          // cos theta_d, sin theta_d, 2 cos theta_d, 2 cos 2 theta_d
         float s0, c0;
-        if constexpr (MODE == kAccurate) {
-            phasor_accurate_off(r1.w, r0.x, r0.z, r1.x, x0, y0, z0, s0, c0);
-        } else {
-            // phase in cycles, the weight's phase first, reduced to
-            // 2 pi (p - rint(p)) for the hardware sin/cos
-            const float p0 = fmaf(r1.x, z0, fmaf(r0.z, y0, fmaf(r0.x, x0, r1.w)));
-            const float th0 = (p0 - rintf(p0)) * kTwoPi;
-            s0 = __sinf(th0);
-            c0 = __cosf(th0);
-        }
-        const float fr = r1.z * c0;  // g_0 = |w| exp(i 2 pi (a.b_0 + phi))
-        const float fi = r1.z * s0;
-        const float gr = fmaf(fr, q.x, -fi * q.y);  // g_1 = g_0 u
-        const float gi = fmaf(fr, q.y, fi * q.x);
-        const f2_t e0 = f2_pack(fr, fi), e1 = f2_pack(gr, gi);
-        const f2_t e2n = f2_fma(f2_pack(-q.z, -q.z), e1, e0);  // -e_2
-        const f2_t e3n = f2_fma(f2_pack(q.z, q.z), e2n, e1);   // -e_3
-        const f2_t kposC = f2_pack(q.w, q.w), knegC = f2_pack(-q.w, -q.w);
-        f2_t amA = e0, aA = e2n, amB = e1, aB = e3n;  // chains over even and odd targets
-        acc[0] = f2_add(acc[0], e0);
-        acc[1] = f2_add(acc[1], e1);
-        acc[2] = f2_add(acc[2], e2n);
-        acc[3] = f2_add(acc[3], e3n);
-#pragma unroll
-        for (int j = 1; 2 * j + 3 < kV; ++j) {
-            const f2_t nA = f2_fma((j & 1) ? kposC : knegC, aA, amA);  // s_{j+1} a_{j+1}
-            const f2_t nB = f2_fma((j & 1) ? kposC : knegC, aB, amB);
-            amA = aA;
-            aA = nA;
-            amB = aB;
-            aB = nB;
-            acc[2 * j + 2] = f2_add(acc[2 * j + 2], aA);
-            acc[2 * j + 3] = f2_add(acc[2 * j + 3], aB);
-        }
+        pre_anchor<MODE>(rec, s, x0, y0, z0, s0, c0);
+        pre_chains(rec, step, s, s0, c0, acc);
     }
 }
 

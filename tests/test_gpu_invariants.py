@@ -260,3 +260,19 @@ def test_concurrent_calls_on_two_streams():
         assert np.array_equal(host_complex(*of), ref_f)
     for w, s in ((wb, s1), (ws_, s2), (wf, s3)):
         assert fhd.fhd_workspace_status(w, s) == 0
+
+
+def test_fma2_rate_probe():
+    """The packed-FMA probe reports a rate between a third of and just above
+    the nominal FP32 lane peak (128 lanes per SM per clock, at most about
+    2.1 GHz), and rejects a null output pointer."""
+    import torch
+
+    import non_cartesian_mri_gather_gb300 as fhd
+
+    rate = ctypes.c_double(0.0)
+    assert fhd.load().fhd_test_fma2_rate(0, ctypes.byref(rate)) == 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nominal_max = sms * 128 * 2.1e9
+    assert nominal_max / 3 < rate.value < 1.05 * nominal_max, rate.value
+    assert fhd.load().fhd_test_fma2_rate(0, None) == 1  # FHD_ERR_INVALID_VALUE
