@@ -94,17 +94,27 @@ def per_pair_counts(path: str):
         # instructions
         return 26.0, 3.0, 18.0
     if path == "source":
-        # the forward gather's source side (segments of S = 32 equally spaced
-        # voxel sources, Cartesian weights) by Horner's rule, groups of G = 8
-        # targets in packed f32x2 pairs: per pair the complex multiply-add
-        # acc = acc z + w as two packed FMAs for the real parts and two for the
-        # imaginary parts of two targets (4 lane operations, 2 instructions);
-        # per (target, segment) the phase of e_0 (3), its reduction and 2 pi t
-        # (4), 2 sin/cos, and e_0 times the segment's sum into the tile sums
-        # (4 lanes; with the pair packing about 13 instructions); per (source,
-        # group) one shared-memory load and the two weight pairs (3); the step
-        # phasor z once per run of segments with the same step (once per tile
-        # on an image grid, not counted).
+        # the fast forward gather's source side (segments of S = 32 equally
+        # spaced voxel sources, Cartesian weights) by Clenshaw's recurrence,
+        # groups of G = 8 targets, each target's (re, im) in one packed pair:
+        # per pair one packed add or subtract and one packed FMA (4 lane
+        # operations, 2 instructions); per (target, segment) the phase of e_0
+        # (3), its reduction and 2 pi t (4), 2 sin/cos, P = y_0 - y_1 / z and
+        # e_0 P into the tile sums (2 packed FMAs each: 8 lanes; with the
+        # swaps and sign pairs about 23 instructions); per (source, group)
+        # one shared-memory load; the step phasor z once per run of segments
+        # with the same step (once per tile on an image grid, not counted).
+        S, G = 32.0, 8.0
+        return 4.0 + 15.0 / S, 2.0 / S, 2.0 + 23.0 / S + 1.0 / G
+    if path == "source-horner":
+        # accurate mode's forward gather: the same segments by Horner's rule,
+        # two targets per packed pair: per pair the complex multiply-add
+        # acc = acc z + w as two packed FMAs for the real parts and two for
+        # the imaginary parts of two targets (4 lane operations, 2
+        # instructions); per (target, segment) the phase of e_0 (3), its
+        # reduction and 2 pi t (4), 2 sin/cos, and e_0 times the segment's sum
+        # into the tile sums (4 lanes; about 13 instructions); per (source,
+        # group) one shared-memory load and the two weight pairs (3).
         S, G = 32.0, 8.0
         return 4.0 + 11.0 / S, 2.0 / S, 2.0 + 13.0 / S + 3.0 / G
     if path == "recurrence-accurate":
@@ -296,9 +306,10 @@ def load_workload(i: int):
 
 def peak_pairs_per_s(sms: int, mhz: float, path: str = "direct") -> float:
     if path == "fhf":
-        # F^H F rho: half the pairs in the forward gather (source side, Horner's
-        # rule), half in the adjoint gather (target recurrence); the bound of
-        # the whole is the pair-weighted harmonic mean of the two.
+        # F^H F rho: half the pairs in the forward gather (source side,
+        # Clenshaw's recurrence), half in the adjoint gather (target
+        # recurrence); the bound of the whole is the pair-weighted harmonic
+        # mean of the two.
         a = peak_pairs_per_s(sms, mhz, "source")
         b = peak_pairs_per_s(sms, mhz, "recurrence")
         return 2.0 / (1.0 / a + 1.0 / b)
@@ -680,7 +691,7 @@ def run_ours(args, world, rank, local):
                        f"{MUFU_LANES_PER_SM}/{n_mufu:g}, {ISSUE_PER_SM}/{n_issue:g}) pairs/clk x "
                        f"{FLOP_PER_PAIR} flop/pair ({path} path)") if path != "fhf" else (
             f"{sms} SMs x {max_mhz:.0f} MHz, pair-weighted harmonic mean of the forward gather's "
-            f"source-side (Horner) bound and the adjoint gather's target-recurrence bound x {FLOP_PER_PAIR} "
+            f"source-side (Clenshaw) bound and the adjoint gather's target-recurrence bound x {FLOP_PER_PAIR} "
             f"flop/pair"),
         "direct_path_peak": FLOP_PER_PAIR * peak_pairs_per_s(sms, max_mhz, "direct") / 1e12,
         # the plain pair-by-pair bound (a sin and a cos per pair), which the

@@ -82,8 +82,10 @@
  *            grid row as sources of F rho; 16 or 32 samples along a straight
  *            line as sources of F^H D), each target evaluates one phasor per
  *            run (two when the run's step changes) and reaches the rest by
- *            powers of the step phasor: Horner's rule in F rho, the same
- *            recurrence in F^H D.  FHD_MODE_DIRECT forces the pair-by-pair
+ *            powers of the step phasor: in F rho Clenshaw's recurrence
+ *            (fast mode; its rounding grows with the run where k.d is near
+ *            an integer or half-integer, within the fast tolerance) or
+ *            Horner's rule (accurate mode), the same recurrence in F^H D.  FHD_MODE_DIRECT forces the pair-by-pair
  *            evaluation everywhere.
  * Small      problems too small to occupy the persistent kernel (a few blocks
  *            of 8192 targets times a few tiles of 256 sources) are evaluated

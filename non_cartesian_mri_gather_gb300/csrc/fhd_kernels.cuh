@@ -92,6 +92,12 @@ namespace fhd {
 #ifndef FHD_UNROLL_PRE
 #define FHD_UNROLL_PRE 6
 #endif
+#ifndef FHD_GOERTZEL
+#define FHD_GOERTZEL 1
+#endif
+#ifndef FHD_GOERTZEL_GROUP
+#define FHD_GOERTZEL_GROUP 8
+#endif
 #ifndef FHD_UNROLL_PRE_ACCURATE
 #define FHD_UNROLL_PRE_ACCURATE 4
 #endif
@@ -628,6 +634,17 @@ __device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
     f2_t d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+__device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b) {
+    f2_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// (hi, lo) of (lo, hi)
+__device__ __forceinline__ f2_t f2_swap(f2_t v) {
+    float lo, hi;
+    f2_unpack(v, lo, hi);
+    return f2_pack(hi, lo);
 }
 
 // ---------------------------------------------------------------- packed pair-by-pair path
@@ -1331,18 +1348,123 @@ __device__ __forceinline__ void accumulate_tile_src_horner(const float4* __restr
     }
 }
 
-// The source-side path of a gather instantiation: Horner's rule in the
-// forward gathers (Cartesian records), whose tiles take this path; the
-// recurrence in the adjoint gathers, where it is rare and where the
-// recurrence measured faster for the kernel as a whole (the fast adjoint
-// kernel inlines this path next to its hot target-side loop).
+// Fast mode's source side in the forward gathers: the segment polynomial
+// P = sum_s w_s z^s of accumulate_tile_src_horner by Clenshaw's recurrence
+// for the basis z^s (z^{s+1} = c z^s - z^{s-1}, c = z + 1/z = 2 cos theta
+// real on the unit circle; Goertzel's algorithm): from the last source down,
+// y_s = w_s + c y_{s+1} - y_{s+2} (y_S = y_{S+1} = 0), then
+// P = y_0 + (z - c) y_1 = y_0 - y_1 / z.  Each target keeps its (re, im)
+// pair packed; with the signs sigma_s = (+, +, -, -, ...) folded into the
+// stored u_s = sigma_s y_s the step is
+// u_s = (sigma_s sigma_{s+1}) c u_{s+1} + (u_{s+2} + sigma_s w_s): one packed
+// add or subtract and one packed FMA per (target, source), the 4 lane
+// operations of Horner's rule, of which half are adds (a packed-add stream
+// keeps the FP32 pipe busier than an FMA-only one).  Clenshaw's recurrence
+// loses accuracy where theta is near 0 or pi (rounding grows like eps S^2
+// there, 1e-4 relative at S = 32); fast mode only, accurate mode keeps
+// Horner's rule.  Per (target, segment): e_0, P from (u_0, u_1) and e_0 P
+// into the tile sums.
+constexpr int kGoertzelGroup = kV < FHD_GOERTZEL_GROUP ? kV : FHD_GOERTZEL_GROUP;
+static_assert(kV % kGoertzelGroup == 0, "Goertzel groups tile the thread's targets");
+
+template <int SEG>
+__device__ __forceinline__ void accumulate_tile_src_goertzel(const float4* __restrict__ rec,
+                                                             const float4* __restrict__ desc,
+                                                             const float (*coord)[kThreads],
+                                                             float (*run)[kThreads], int tid) {
+    constexpr int G = kGoertzelGroup;
+#pragma unroll 1
+    for (int g = 0; g < kV; g += G) {
+        float bx[G], by[G], bz[G];
+#pragma unroll
+        for (int v = 0; v < G; ++v) {
+            bx[v] = coord[g + v][tid];
+            by[v] = coord[kV + g + v][tid];
+            bz[v] = coord[2 * kV + g + v][tid];
+        }
+        f2_t acc[G];                // tile sums (re, im) of each target
+        f2_t kp[G], kn[G];          // (c, c) and (-c, -c), c = 2 cos theta
+        float zr[G], zi[G];         // z = exp(i theta)
+#pragma unroll
+        for (int v = 0; v < G; ++v) acc[v] = 0ull;  // +0.0f in both halves
+        float4 d_prev = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int j = 0; j < kTile / SEG; ++j) {
+            const float4 d = desc[j];
+            if (j == 0 || d.x != d_prev.x || d.y != d_prev.y || d.z != d_prev.z) {  // uniform over the CTA
+                // z from the phasor of half the step, as in Horner's rule
+                const float hx = 0.5f * d.x, hy = 0.5f * d.y, hz = 0.5f * d.z;
+#pragma unroll
+                for (int v = 0; v < G; ++v) {
+                    float sh, ch;
+                    phasor_mufu(fmaf(hz, bz[v], fmaf(hy, by[v], hx * bx[v])), sh, ch);
+                    zr[v] = fmaf(-2.0f * sh, sh, 1.0f);
+                    zi[v] = (sh + sh) * ch;
+                    const float c = zr[v] + zr[v];
+                    kp[v] = f2_pack(c, c);
+                    kn[v] = f2_pack(-c, -c);
+                }
+                d_prev = d;
+            }
+            f2_t u1[G], u2[G];  // u_{s+1}, u_{s+2}
+#pragma unroll
+            for (int v = 0; v < G; ++v) {
+                u1[v] = 0ull;
+                u2[v] = 0ull;
+            }
+#pragma unroll
+            for (int s = SEG - 1; s >= 0; --s) {
+                const float4 r = rec[2 * (j * SEG + s) + 1];  // the weight in .z, .w
+                const f2_t w = f2_pack(r.z, r.w);
+#pragma unroll
+                for (int v = 0; v < G; ++v) {
+                    const f2_t t = (s & 2) ? f2_sub(u2[v], w) : f2_add(u2[v], w);  // u_{s+2} + sigma_s w_s
+                    const f2_t u = f2_fma((s & 1) ? kn[v] : kp[v], u1[v], t);        // sigma_s sigma_{s+1} = +-1
+                    u2[v] = u1[v];
+                    u1[v] = u;
+                }
+            }
+            // u1 = u_0 = y_0, u2 = u_1 = y_1 (sigma_0 = sigma_1 = +1)
+            const float4 b0 = rec[2 * j * SEG];      // A_0.x A_0.x A_0.y A_0.y
+            const float4 b1 = rec[2 * j * SEG + 1];  // A_0.z A_0.z w
+#pragma unroll
+            for (int v = 0; v < G; ++v) {
+                float s0, c0;
+                phasor_mufu(fmaf(b1.x, bz[v], fmaf(b0.z, by[v], b0.x * bx[v])), s0, c0);
+                // P = y_0 - y_1 / z = y_0 - conj(z) y_1
+                const f2_t t = f2_fma(f2_pack(-zr[v], -zr[v]), u2[v], u1[v]);
+                const f2_t P = f2_fma(f2_pack(-zi[v], zi[v]), f2_swap(u2[v]), t);
+                // acc += e_0 P
+                acc[v] = f2_fma(f2_pack(c0, c0), P, f2_fma(f2_pack(-s0, s0), f2_swap(P), acc[v]));
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < G; ++v) {
+            float re, im;
+            f2_unpack(acc[v], re, im);
+            run[g + v][tid] += re;
+            run[kV + g + v][tid] += im;
+        }
+    }
+}
+
+// The source-side path of a gather instantiation: in the forward gathers
+// (Cartesian records), whose tiles take this path, Clenshaw's recurrence in
+// fast mode and Horner's rule in accurate mode; the recurrence in the
+// adjoint gathers, where it is rare and where the recurrence measured faster
+// for the kernel as a whole (the fast adjoint kernel inlines this path next
+// to its hot target-side loop).
 template <int MODE, int SEG, bool POLAR>
 __device__ __forceinline__ void source_tile(const float4* __restrict__ rec, const float4* __restrict__ desc,
                                             const float (*coord)[kThreads], float (*run)[kThreads], int tid) {
-    if constexpr (!POLAR)
-        accumulate_tile_src_horner<MODE, SEG, POLAR>(rec, desc, coord, run, tid);
-    else
+    if constexpr (!POLAR) {
+        if constexpr (MODE == kFast && FHD_GOERTZEL)
+            accumulate_tile_src_goertzel<SEG>(rec, desc, coord, run, tid);
+        else
+            accumulate_tile_src_horner<MODE, SEG, POLAR>(rec, desc, coord, run, tid);
+    } else {
         accumulate_tile_src_strided<MODE, SEG, POLAR>(rec, desc, coord, run, tid);
+    }
 }
 
 // Out-of-line entry points of the pair-by-pair and source-side paths.  The

@@ -50,7 +50,7 @@ def test_roofline_counts():
     # accurate pair by pair: 26 FP32 lane operations per pair bind
     lanes, xu, issue = bench.per_pair_counts("direct-accurate")
     assert abs(bench.peak_pairs_per_s(152, 2070.0, "direct-accurate") - 152 * (128 / lanes) * 2070e6) < 1
-    for path in ("source", "recurrence-accurate", "recurrence-accurate-shared"):
+    for path in ("source", "source-horner", "recurrence-accurate", "recurrence-accurate-shared"):
         assert all(v > 0 for v in bench.per_pair_counts(path))
     # the step records take work off the accurate recurrence too
     assert bench.per_pair_counts("recurrence-accurate")[0] < bench.per_pair_counts("recurrence-accurate-shared")[0]
