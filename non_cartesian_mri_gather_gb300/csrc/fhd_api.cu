@@ -88,11 +88,41 @@ bool overlaps(const Buf& a, const Buf& b) {
     return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
 }
 
-// Device-memory, alignment and allocation-range checks for one array.
+typedef CUresult(CUDAAPI* PFN_attrs)(unsigned int, CUpointer_attribute*, void**, CUdeviceptr);
+
+// Device-memory, alignment and allocation-range checks for one array: one
+// driver query (cuPointerGetAttributes) for the memory type, device,
+// managed flag and the allocation's range; where that entry point cannot be
+// resolved, the runtime's pointer attributes and cuMemGetAddressRange.
 fhd_status check_array(const void* p, size_t bytes, size_t align, int device) {
     if (bytes == 0) return FHD_OK;
     if (p == nullptr) return FHD_ERR_INVALID_VALUE;
     if ((uintptr_t)p % align != 0) return FHD_ERR_MISALIGNED;
+    // Driver entry point, resolved once per process (thread-safe static init).
+    static const PFN_attrs attrs_fn = [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const bool ok = cudaGetDriverEntryPointByVersion("cuPointerGetAttributes", &fn, 12000, cudaEnableDefault,
+                                                         &q) == cudaSuccess &&
+                        q == cudaDriverEntryPointSuccess;
+        cudaGetLastError();
+        return ok ? (PFN_attrs)fn : (PFN_attrs) nullptr;
+    }();
+    if (attrs_fn) {
+        // each slot zeroed and wider than the value the driver writes into it
+        unsigned long long memtype = 0, managed = 0, start = 0, size = 0;
+        int ordinal = -1;
+        CUpointer_attribute which[5] = {CU_POINTER_ATTRIBUTE_MEMORY_TYPE, CU_POINTER_ATTRIBUTE_DEVICE_ORDINAL,
+                                        CU_POINTER_ATTRIBUTE_IS_MANAGED, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR,
+                                        CU_POINTER_ATTRIBUTE_RANGE_SIZE};
+        void* data[5] = {&memtype, &ordinal, &managed, &start, &size};
+        // a pointer CUDA does not know gets zero attributes, not an error
+        if (attrs_fn(5, which, data, (CUdeviceptr)(uintptr_t)p) != CUDA_SUCCESS) return FHD_ERR_INVALID_VALUE;
+        if (managed == 0 && ((CUmemorytype)memtype != CU_MEMORYTYPE_DEVICE || ordinal != device))
+            return FHD_ERR_INVALID_VALUE;
+        if (size != 0 && (uintptr_t)p + bytes > (uintptr_t)start + size) return FHD_ERR_RANGE;
+        return FHD_OK;
+    }
     cudaPointerAttributes attr;
     if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
         cudaGetLastError();

@@ -1080,6 +1080,17 @@ __device__ __forceinline__ bool equally_spaced(const float (&c)[kV], int n, floa
         d = 0.f;
         return true;
     }
+    if (c[1] == c[0]) {
+        // spacing 0 (a coordinate that is constant along a grid row): the
+        // condition is c[v] == c[0], exact in float32 (and this GPU's double
+        // rate is a small fraction of its float rate)
+        d = 0.f;
+        bool ok = true;
+#pragma unroll
+        for (int v = 2; v < kV; ++v)
+            if (v < n) ok = ok && c[v] == c[0];
+        return ok;
+    }
     const double c0 = c[0];
     const double dd = (double)c[1] - c0;
     d = (float)dd;
