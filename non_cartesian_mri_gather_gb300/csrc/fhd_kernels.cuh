@@ -21,6 +21,10 @@
 //                       records to a whole number of tiles.  The
 //                       array-of-structures record follows the mtuann notes'
 //                       step 4 and the SampleChunk struct of section 17.3.4.
+//                       For the adjoint sum it also writes one step record
+//                       per source: the step phasor and chain coefficients of
+//                       the target-side recurrence for the voxels' common
+//                       spacing, in double.
 //   2. gather_kernel  - persistent CTAs; each owns an equal contiguous range
 //                       of (target block, source tile) work items.  A
 //                       producer warp streams source tiles into a shared-
@@ -32,12 +36,15 @@
 //                       section 17.3.3) and write every output once.  Per warp
 //                       and tile one of three paths: equally spaced targets
 //                       take a recurrence instead of a sin/cos per pair
-//                       (accumulate_tile_strided); otherwise tiles of equally
-//                       spaced source segments (described by
+//                       (accumulate_tile_pre with the staged step records
+//                       where the warp's spacing is the launch's common one,
+//                       accumulate_tile_strided otherwise); otherwise tiles
+//                       of equally spaced source segments (described by
 //                       describe_segments) a source-side evaluation
-//                       (source_tile: Horner's rule in the forward gather, a
-//                       recurrence in the adjoint gather); otherwise pair by
-//                       pair (direct_tile).  Instantiated per mode, source
+//                       (source_tile: Clenshaw's recurrence in fast mode and
+//                       Horner's rule in accurate mode in the forward gather,
+//                       a recurrence in the adjoint gather); otherwise pair
+//                       by pair (direct_tile).  Instantiated per mode, source
 //                       segment length and weight form: the adjoint gathers
 //                       (polar weights) and the forward gathers (Cartesian
 //                       weights) of each mode.
