@@ -364,10 +364,10 @@ def _spokes(n_spokes, seed, points=256):
 @pytest.mark.parametrize("mode", ALL_MODES)
 @pytest.mark.parametrize("drop", [0, 5])
 def test_fwd_grid_voxel_sources(side, mode, drop):
-    """F rho with the voxels of a side^3 grid as sources: rows of 32 split into
-    equally spaced segments of 16 (fast mode) or 32 (accurate mode) sources
-    (source recurrence); rows of 24 make segments straddle rows, so those
-    tiles are evaluated pair by pair.  drop = 5 leaves the last segment with
+    """F rho with the voxels of a side^3 grid as sources: rows of 32 are
+    equally spaced segments of 32 sources (Clenshaw's recurrence in fast
+    mode, Horner's rule in accurate mode); rows of 24 make segments straddle
+    rows, so those tiles are evaluated pair by pair.  drop = 5 leaves the last segment with
     fewer real sources than its length (the rest zero-weight padding)."""
     from inputs import grid_coords
 
@@ -376,6 +376,29 @@ def test_fwd_grid_voxel_sources(side, mode, drop):
     p.x, p.y, p.z = x, y, z
     ref = oracle.forward(p.x, p.y, p.z, p.rho_r + 1j * p.rho_i, p.kx, p.ky, p.kz)
     check(gpu_fwd(p, mode), ref, mode, f"F rho, {side}^3 voxel sources")
+
+
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_fwd_step_angle_extremes(mode):
+    """F rho on a 64^3 grid with samples whose step angle along a voxel row,
+    theta = 2 pi k_x / 64, is 0, pi or 2 pi, or just off them: there fast
+    mode's Clenshaw recurrence rounds worst (its error grows like eps S^2
+    over a segment of S = 32 sources, about 1e-4 relative at worst in a
+    float32 emulation), while accurate mode's Horner's rule is unaffected.
+    The fast bound here is tighter than the mode's tolerance, so a change
+    that makes the recurrence lose more shows."""
+    from inputs import grid_coords
+
+    base = np.array([0.0, 32.0, -32.0, 64.0, -64.0])
+    kx = np.concatenate([base, base + 1e-3, base - 1e-3, base + 0.01])
+    p = random_problem(64 ** 3, kx.size, kmax=32.0, seed=41, op="fwd")
+    p.x, p.y, p.z = grid_coords(64, 64, 64)
+    p.kx = kx.astype(np.float32)
+    ref = oracle.forward(p.x, p.y, p.z, p.rho_r + 1j * p.rho_i, p.kx, p.ky, p.kz)
+    got = gpu_fwd(p, mode)
+    check(got, ref, mode, "F rho at step angles 0 and pi")
+    if mode == FAST:
+        assert rel_l2(got, ref) <= 2e-4, f"fast relL2 {rel_l2(got, ref):.3e}"
 
 
 @pytest.mark.parametrize("mode", [ACC, FAST])
