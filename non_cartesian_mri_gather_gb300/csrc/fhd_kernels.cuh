@@ -97,7 +97,7 @@ namespace fhd {
 #define FHD_HORNER_GROUP 8
 #endif
 #ifndef FHD_UNROLL_PRE
-#define FHD_UNROLL_PRE 6
+#define FHD_UNROLL_PRE 3
 #endif
 #ifndef FHD_GOERTZEL
 #define FHD_GOERTZEL 1
@@ -136,6 +136,7 @@ constexpr int kUnrollSharedU = 12;       // the same in the accurate warp-shared
 constexpr int kUnrollTwoChains = 6;
 constexpr int kUnrollOneChain = 3;
 // the same with the staged step records (accumulate_tile_pre), per mode
+// (measured best: 3 of 1-8 in fast mode, 4 of 2-8 in accurate mode)
 constexpr int kUnrollPreFast = FHD_UNROLL_PRE;
 constexpr int kUnrollPreAccurate = FHD_UNROLL_PRE_ACCURATE;
 // The adjoint gathers store each weight in polar form, {|w|, arg(w) / 2 pi}
