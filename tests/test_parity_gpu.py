@@ -317,6 +317,24 @@ def test_step_records_differ_but_both_match(mode):
     assert not np.array_equal(a, b), "the step records were not used"
 
 
+@pytest.mark.parametrize("mode", [ACC, FAST])
+def test_step_records_for_a_spacing_no_warp_has(mode):
+    """A 32^3 grid whose first voxel is moved off the grid: the launch's
+    common spacing (that of the first two voxels) is then one no thread has,
+    so the step records apply to no warp; the first warp's first thread is
+    not equally spaced (that warp evaluates pair by pair) and every other
+    warp evaluates its own step phasor.  All match the oracle."""
+    p = random_problem(32768, 1500, kmax=30.0, seed=18, coords="grid")
+    p.x = p.x.copy()
+    p.x[0] = np.float32(-0.4871)
+    ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
+    got = gpu_fhd(p, mode)
+    check(got, ref, mode, "F^H D, common spacing of no warp")
+    with step_records(0):
+        alone = gpu_fhd(p, mode)
+    assert np.array_equal(got, alone), "step records were used where no warp has their spacing"
+
+
 def test_recurrence_and_direct_differ_but_both_match():
     p = random_problem(32768, 2000, kmax=32.0, seed=6, coords="grid")  # a 32^3 grid: exact spacing
     ref = oracle.adjoint(p.kx, p.ky, p.kz, p.Dr + 1j * p.Di, p.x, p.y, p.z)
