@@ -233,7 +233,8 @@ FHD_API fhd_status fhd_launch_shape(int device, fhd_mode mode, int *ctas, int *t
  * F^H D without any allocation, for callers that cannot allocate device
  * memory.  The operation, argument meaning, layout, validation and results
  * are those of fhd_compute, but there is no workspace argument: the scratch
- * space (packed sample records, per-CTA partial sums, status word) is a
+ * space (packed sample records and step records, per-CTA partial sums,
+ * status word) is a
  * file-scope static device array of FHD_NOALLOC_SCRATCH_BYTES inside the
  * library.  The pages this library implements have no counterpart of this
  * entry point; it exists for deployment.
